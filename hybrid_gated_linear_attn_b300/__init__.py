@@ -1,0 +1,13 @@
+"""Lizard hybrid attention operator (gated linear attention + anchor window
+with meta-memory sinks) as hand-written CUDA for B300 (sm_103a), behind the
+C ABI of ``include/lizard_attn.h``.
+"""
+from .lizard_attn import (  # noqa: F401
+    LizardError,
+    LizardState,
+    lizard_attn_decode_step,
+    lizard_attn_prefill,
+    lizard_check_device_status,
+    lizard_state_init,
+    lizard_status_string,
+)

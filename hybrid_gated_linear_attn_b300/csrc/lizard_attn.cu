@@ -1,0 +1,175 @@
+// lizard_attn.cu -- C ABI of the Lizard hybrid attention operator.
+//
+// Host-side validation and launch of the kernels in decode.cuh,
+// prefill_simt.cuh and the state initialiser below.  Declarations and the
+// contract of every entry point are in include/lizard_attn.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/lizard_attn.h"
+#include "common.cuh"
+#include "decode.cuh"
+#include "prefill_simt.cuh"
+
+namespace lizard {
+
+__global__ void state_init_kernel(float *S, size_t nS, uint4 *ring_k, uint4 *ring_v, size_t nring16,
+                                  int64_t *pos, int B)
+{
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t i = i0; i < nS / 4; i += stride) reinterpret_cast<float4 *>(S)[i] = z4;
+    const uint4 zu = make_uint4(0, 0, 0, 0);
+    for (size_t i = i0; i < nring16; i += stride) {
+        ring_k[i] = zu;
+        ring_v[i] = zu;
+    }
+    for (size_t i = i0; i < (size_t)B; i += stride) pos[i] = 0;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static size_t esize(lizard_dtype dt) { return dt == LIZARD_F32 ? 4 : 2; }
+static bool dtype_ok(lizard_dtype dt) { return dt == LIZARD_F32 || dt == LIZARD_BF16; }
+
+static lizard_status check_state(const lizard_state *st)
+{
+    if (!st) return LIZARD_ERR_INVALID_ARG;
+    if (!dtype_ok(st->dtype)) return LIZARD_ERR_INVALID_ARG;
+    if (st->B < 0 || st->H < 1 || st->dk < 1 || st->dv < 1 || st->w < 1) return LIZARD_ERR_INVALID_ARG;
+    if (!st->S || !st->ring_k || !st->ring_v || !st->pos) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(st->S) || !aligned16(st->ring_k) || !aligned16(st->ring_v) || !aligned16(st->pos))
+        return LIZARD_ERR_INVALID_ARG;
+    if (st->dk != st->dv || (st->dk != 64 && st->dk != 128)) return LIZARD_ERR_UNSUPPORTED;
+    if (st->w > LIZARD_MAX_WINDOW) return LIZARD_ERR_UNSUPPORTED;
+    return LIZARD_OK;
+}
+
+static lizard_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
+}
+
+template <typename T, int D>
+static lizard_status launch_prefill(const PrefillArgs &pa, cudaStream_t s)
+{
+    const size_t smem = prefill_simt_smem_bytes<D>(pa.w, pa.m);
+    auto kern = prefill_simt_kernel<T, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    kern<<<pa.B * pa.H, SIMT_THREADS, smem, s>>>(pa);
+    return launch_status();
+}
+
+template <typename T, int D>
+static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
+{
+    const size_t smem = decode_smem_bytes<D>(da.w, da.m);
+    auto kern = decode_step_kernel<T, D>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    kern<<<da.B * da.H, DECODE_THREADS, smem, s>>>(da);
+    if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
+    advance_pos_kernel<<<(da.B + 255) / 256, 256, 0, s>>>(const_cast<int64_t *>(da.pos), da.B);
+    return launch_status();
+}
+
+}  // namespace lizard
+
+using namespace lizard;
+
+extern "C" {
+
+const char *lizard_status_string(lizard_status s)
+{
+    switch (s) {
+    case LIZARD_OK: return "LIZARD_OK";
+    case LIZARD_ERR_INVALID_ARG: return "LIZARD_ERR_INVALID_ARG";
+    case LIZARD_ERR_UNSUPPORTED: return "LIZARD_ERR_UNSUPPORTED";
+    case LIZARD_ERR_CUDA: return "LIZARD_ERR_CUDA";
+    case LIZARD_ERR_TIMEOUT: return "LIZARD_ERR_TIMEOUT";
+    }
+    return "LIZARD_ERR_UNKNOWN";
+}
+
+lizard_status lizard_state_init(const lizard_state *st, lizard_stream_t stream)
+{
+    lizard_status rc = check_state(st);
+    if (rc != LIZARD_OK) return rc;
+    const size_t nS = (size_t)st->B * st->H * st->dk * st->dv;
+    const size_t ring_bytes = (size_t)st->B * st->H * st->w * st->dk * esize(st->dtype);
+    if (st->B == 0) return LIZARD_OK;
+    int blocks = (int)((nS / 4 + 255) / 256);
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    state_init_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+        st->S, nS, static_cast<uint4 *>(st->ring_k), static_cast<uint4 *>(st->ring_v), ring_bytes / 16, st->pos,
+        st->B);
+    return launch_status();
+}
+
+lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
+                                  float alpha, int B, int H, int L, int dk, int dv, int w, int m,
+                                  lizard_dtype dtype, void *y, const lizard_state *st, lizard_stream_t stream)
+{
+    if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
+    if (B < 0 || H < 1 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0) return LIZARD_ERR_INVALID_ARG;
+    // An empty prompt (L == 0) has no token tensors to point at.
+    if (L > 0 && (!q || !k || !v || !g || !y)) return LIZARD_ERR_INVALID_ARG;
+    if (m > 0 && !meta_k) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(y) ||
+        (m > 0 && !aligned16(meta_k)))
+        return LIZARD_ERR_INVALID_ARG;
+    if (dk != dv || (dk != 64 && dk != 128)) return LIZARD_ERR_UNSUPPORTED;
+    if (w > LIZARD_MAX_WINDOW || m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
+    if (st) {
+        lizard_status rc = check_state(st);
+        if (rc != LIZARD_OK) return rc;
+        if (st->B != B || st->H != H || st->dk != dk || st->dv != dv || st->w != w || st->dtype != dtype)
+            return LIZARD_ERR_INVALID_ARG;
+    }
+    if (B == 0) return LIZARD_OK;
+    PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m,
+                   st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
+                   st ? st->pos : nullptr};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == LIZARD_BF16)
+        return dk == 128 ? launch_prefill<__nv_bfloat16, 128>(pa, s) : launch_prefill<__nv_bfloat16, 64>(pa, s);
+    return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
+}
+
+lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
+                                      float alpha, int m, void *y, const lizard_state *st, lizard_stream_t stream)
+{
+    lizard_status rc = check_state(st);
+    if (rc != LIZARD_OK) return rc;
+    if (m < 0) return LIZARD_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !y || (m > 0 && !meta_k)) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(y) ||
+        (m > 0 && !aligned16(meta_k)))
+        return LIZARD_ERR_INVALID_ARG;
+    if (m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    if (st->B == 0) return LIZARD_OK;
+    DecodeArgs da{q, k, v, g, meta_k, y, st->S, st->ring_k, st->ring_v, st->pos, alpha, st->B, st->H, st->w, m};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (st->dtype == LIZARD_BF16)
+        return st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s) : launch_decode<__nv_bfloat16, 64>(da, s);
+    return st->dk == 128 ? launch_decode<float, 128>(da, s) : launch_decode<float, 64>(da, s);
+}
+
+lizard_status lizard_check_device_status(lizard_stream_t stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LIZARD_ERR_CUDA;
+    int word = DEV_OK, zero = DEV_OK;
+    if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof word) != cudaSuccess) return LIZARD_ERR_CUDA;
+    if (word != DEV_OK && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    if (word == DEV_OK) return LIZARD_OK;
+    return word == DEV_BAD_POS ? LIZARD_ERR_INVALID_ARG : LIZARD_ERR_TIMEOUT;
+}
+
+}  // extern "C"

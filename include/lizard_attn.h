@@ -1,0 +1,149 @@
+/*
+ * lizard_attn.h -- C ABI of the Lizard hybrid attention operator on B300.
+ *
+ *     y_t = yg_t + alpha * ya_t
+ *
+ * "Lizard: An Efficient Linearization Framework for Large Language Models"
+ * (gist.science/de), section 2 "Kernkomponenten der Architektur":
+ *   item 1 "Gated Linear Attention (GLA) mit lernbarem Gate" -- the gate
+ *          branch yg, a recurrence over a d_k x d_v state per head whose
+ *          rows decay by sigmoid(g_t), the learnable data-dependent gate:
+ *              S_t = diag(sigmoid(g_t)) S_{t-1} + k_t^T v_t ,   yg_t = q_t S_t
+ *   item 2 "Anchor Window Attention" -- the anchor branch ya, softmax
+ *          attention over the w most recent tokens (the current one
+ *          included) plus m learnable meta-memory keys that act as attention
+ *          sinks: they enter the softmax normaliser and carry value zero:
+ *              ya_t = sum_s e^{q_t.k_s} v_s / (sum_s e^{q_t.k_s} + sum_j e^{q_t.mu_j})
+ *   item 3 "Hybride Ausgabe" -- the combine y = yg + alpha * ya.
+ * The same operator is described in gist.science/it section 2 "Architettura
+ * Ibrida" and gist.science/pt section 2A "Arquitetura Hibrida".  No scale is
+ * applied inside the softmax: callers pre-scale q (and k) as they wish.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or retains them past the call.
+ *   - Tensors are dense, row-major, head-major: [B][H][L][d] with the last
+ *     dimension contiguous.  Every pointer must be 16-byte aligned.
+ *   - Element type of q, k, v, g, meta keys, y and the ring buffer is the
+ *     call's lizard_dtype (fp32 or bf16).  The recurrent state S is always
+ *     fp32 and all accumulation is fp32.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream); a call returns once the work is enqueued.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and touches no buffer.
+ *   - Errors are returned as lizard_status.  Nothing aborts, throws or traps.
+ *   - Supported shapes: d_k == d_v in {64, 128}; 1 <= w <= LIZARD_MAX_WINDOW;
+ *     0 <= m <= LIZARD_MAX_META.  Anything else in range but not built is
+ *     LIZARD_ERR_UNSUPPORTED; anything meaningless is LIZARD_ERR_INVALID_ARG.
+ */
+#ifndef LIZARD_ATTN_H
+#define LIZARD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LIZARD_API __attribute__((visibility("default")))
+#else
+#define LIZARD_API
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers (same type). */
+struct CUstream_st;
+typedef struct CUstream_st *lizard_stream_t;
+
+#define LIZARD_MAX_WINDOW 256
+#define LIZARD_MAX_META 16
+
+typedef enum {
+    LIZARD_OK = 0,
+    LIZARD_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or dtype */
+    LIZARD_ERR_UNSUPPORTED = 2,   /* valid request outside the built shapes    */
+    LIZARD_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed       */
+    LIZARD_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up         */
+} lizard_status;
+
+typedef enum { LIZARD_F32 = 0, LIZARD_BF16 = 1 } lizard_dtype;
+
+/*
+ * Recurrent state of B sequences x H heads: what constant-memory decoding
+ * keeps between tokens (gist.science/de section 2 item 1, last bullet).
+ *   S       [B][H][dk][dv] fp32   gate-branch state, row i = key dim i
+ *   ring_k  [B][H][w][dk]  dtype  keys of the last w tokens, token p in slot p % w
+ *   ring_v  [B][H][w][dv]  dtype  values, same slots
+ *   pos     [B] int64             tokens consumed so far by each sequence
+ * All four are caller-owned device buffers.
+ */
+typedef struct {
+    float *S;
+    void *ring_k;
+    void *ring_v;
+    int64_t *pos;
+    int B, H, dk, dv, w;
+    lizard_dtype dtype;
+} lizard_state;
+
+/*
+ * lizard_state_init: the empty state -- S = 0, ring = 0, pos = 0 -- for all
+ * B x H units.  Enqueued on `stream`.  Errors: INVALID_ARG for a null state
+ * or buffer, bad sizes or misaligned buffers; CUDA if the launch fails.
+ */
+LIZARD_API lizard_status lizard_state_init(const lizard_state *st, lizard_stream_t stream);
+
+/*
+ * lizard_attn_prefill: the operator over a whole prompt of L tokens per
+ * sequence, starting from the empty state (no earlier tokens).
+ *   q, k, g  [B][H][L][dk]  dtype   queries, keys, gate logits (gamma = sigmoid(g))
+ *   v        [B][H][L][dv]  dtype   values
+ *   meta_k   [H][m][dk]     dtype   meta-memory keys (may be NULL when m == 0)
+ *   alpha                           weight of the anchor branch
+ *   y        [B][H][L][dv]  dtype   output (written; may not alias an input)
+ *   st       nullable.  When given, its dims/dtype must match the call and
+ *            the prefill WRITES the state that follows the prompt: S after
+ *            token L-1, the last min(L, w) keys/values into the ring, and
+ *            pos[b] = L.  Its previous contents are ignored.
+ * L == 0 or B*H == 0 is a valid empty call (only the state is written);
+ * with L == 0 the token pointers (q, k, v, g, y) may be NULL.
+ */
+LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, const void *g,
+                                  const void *meta_k, float alpha,
+                                  int B, int H, int L, int dk, int dv, int w, int m,
+                                  lizard_dtype dtype, void *y, const lizard_state *st,
+                                  lizard_stream_t stream);
+
+/*
+ * lizard_attn_decode_step: one new token for each of st->B sequences and
+ * st->H heads, continuing from `st` (updated in place).
+ *   q, k, g  [B][H][dk]  st->dtype;  v [B][H][dv];  meta_k [H][m][dk]
+ *   y        [B][H][dv]  st->dtype   output
+ * At p = pos[b]: S <- diag(sigmoid(g)) S + k^T v; yg = q S; the window is the
+ * current token plus tokens max(0, p-w+1) .. p-1 read from the ring; then
+ * the current k, v go to ring slot p % w and pos[b] becomes p + 1.
+ * Enqueues two kernels (the step, then the pos advance).
+ */
+LIZARD_API lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g,
+                                      const void *meta_k, float alpha, int m, void *y,
+                                      const lizard_state *st, lizard_stream_t stream);
+
+/*
+ * lizard_check_device_status: synchronises `stream`, then reads and clears
+ * the library's device error word.  LIZARD_ERR_TIMEOUT if a kernel since the
+ * last check abandoned a bounded wait (its outputs are then undefined),
+ * LIZARD_ERR_INVALID_ARG if a decode step found a negative pos (that
+ * sequence's outputs and state were left untouched), LIZARD_ERR_CUDA if
+ * synchronising failed, LIZARD_OK otherwise.
+ */
+LIZARD_API lizard_status lizard_check_device_status(lizard_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+LIZARD_API const char *lizard_status_string(lizard_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIZARD_ATTN_H */

@@ -1,0 +1,101 @@
+"""CUDA decode step against the fp64 oracle's decode step and against the
+oracle's prefill of the whole sequence (bf16: rel L2 <= 1e-2)."""
+import pytest
+import torch
+
+from hybrid_gated_linear_attn_b300 import LizardState, lizard_state_init
+from hybrid_gated_linear_attn_b300.inputs import (WORKLOADS, decode_initial_state, decode_step_inputs,
+                                                  prefill_inputs, rel_l2, torch_dtype)
+from oracle import oracle as O
+from tests.gpu_helpers import TOL, ensure_built, gpu_decode_step, gpu_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _gpu_state_from(init: dict, wl) -> LizardState:
+    st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=init["ring_k"].dtype)
+    st.S.copy_(init["S"])
+    st.ring_k.copy_(init["ring_k"])
+    st.ring_v.copy_(init["ring_v"])
+    st.pos.copy_(init["pos"])
+    return st
+
+
+def _run_decode(wl, steps, seq=None):
+    init = decode_initial_state(wl)
+    st = _gpu_state_from(init, wl)
+    seq = list(range(wl.B)) if seq is None else seq
+    ost = dict(S=init["S"][seq].double().contiguous(), ring_k=init["ring_k"][seq].contiguous(),
+               ring_v=init["ring_v"][seq].contiguous(), pos=init["pos"][seq].clone())
+    worst = 0.0
+    for s in range(steps):
+        inp = decode_step_inputs(wl, s)
+        y = gpu_decode_step(inp, init["mu"], wl.alpha, st).cpu()
+        sub = {n: inp[n][seq].contiguous() for n in ("q", "k", "v", "g")}
+        y_ref = O.decode_step(sub["q"], sub["k"], sub["v"], sub["g"], init["mu"], wl.alpha, ost)
+        err = rel_l2(y[seq], y_ref)
+        worst = max(worst, err)
+        assert err <= TOL[inp["q"].dtype], f"step {s}: rel L2 {err:.3e}"
+    errS = rel_l2(st.S.cpu()[seq], ost["S"])
+    assert errS <= TOL[torch_dtype(wl.dtype)], f"state rel L2 {errS:.3e}"
+    assert torch.all(st.pos.cpu() == init["pos"] + steps)
+    for b_local, b in enumerate(seq):
+        assert torch.equal(st.ring_k.cpu()[b], ost["ring_k"][b_local])
+        assert torch.equal(st.ring_v.cpu()[b], ost["ring_v"][b_local])
+    return worst
+
+
+@pytest.mark.parametrize("d,w,m,hist,dtype", [
+    (128, 64, 4, 64, "bf16"),     # full ring
+    (128, 64, 4, 10, "bf16"),     # ring still filling (pos < w)
+    (64, 16, 0, 40, "f32"),       # no sinks
+    (64, 1, 3, 5, "f32"),         # window of one token
+    (128, 256, 16, 300, "bf16"),  # largest window and meta count
+])
+def test_decode_small(d, w, m, hist, dtype):
+    wl = WORKLOADS["decode"].replace(B=3, H=4, dk=d, dv=d, w=w, m=m, L=hist, dtype=dtype)
+    _run_decode(wl, steps=2 * w + 3)
+
+
+def test_decode_from_empty_state():
+    wl = WORKLOADS["decode"].replace(B=2, H=3, L=0)
+    st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=torch.bfloat16)
+    lizard_state_init(st)
+    torch.cuda.synchronize()
+    assert torch.all(st.S.cpu() == 0) and torch.all(st.pos.cpu() == 0)
+    init = decode_initial_state(wl)
+    ost = dict(S=torch.zeros(wl.B, wl.H, wl.dk, wl.dv, dtype=torch.float64),
+               ring_k=torch.zeros_like(init["ring_k"]), ring_v=torch.zeros_like(init["ring_v"]),
+               pos=torch.zeros(wl.B, dtype=torch.int64))
+    for s in range(5):
+        inp = decode_step_inputs(wl, s)
+        y = gpu_decode_step(inp, init["mu"], wl.alpha, st).cpu()
+        y_ref = O.decode_step(inp["q"], inp["k"], inp["v"], inp["g"], init["mu"], wl.alpha, ost)
+        assert rel_l2(y, y_ref) <= 1e-2
+
+
+def test_decode_workload_full_size_sampled():
+    """64 sequences x H32 d128 bf16, w64 m4, 1024 steps in one state; the
+    oracle follows sequences 0 and 37 for every step."""
+    wl = WORKLOADS["decode"]
+    _run_decode(wl, steps=wl.decode_steps, seq=[0, 37])
+
+
+@pytest.mark.parametrize("L,w,n", [(100, 64, 9), (20, 64, 70), (130, 16, 5)])
+def test_prefill_then_decode_equals_longer_prefill(L, w, n):
+    wl = WORKLOADS["llama3_8b"].replace(B=2, H=3, L=L + n, w=w, seed=L)
+    inp = prefill_inputs(wl)
+    head = {k: (v[:, :, :L].contiguous() if isinstance(v, torch.Tensor) and k != "mu" else v)
+            for k, v in inp.items()}
+    _, st = gpu_prefill(head, w)
+    y_ref = O.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], w)
+    for t in range(L, L + n):
+        step = {k: inp[k][:, :, t].contiguous() for k in ("q", "k", "v", "g")}
+        y = gpu_decode_step(step, inp["mu"], inp["alpha"], st).cpu()
+        err = rel_l2(y, y_ref[:, :, t])
+        assert err <= 1e-2, f"t={t}: rel L2 {err:.3e}"
