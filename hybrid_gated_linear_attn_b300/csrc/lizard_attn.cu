@@ -1,7 +1,8 @@
 // lizard_attn.cu -- C ABI of the Lizard hybrid attention operator.
 //
 // Host-side validation and launch of the kernels in decode.cuh,
-// prefill_simt.cuh and the state initialiser below.  Declarations and the
+// prefill_tc.cuh (bf16, d = 128: tensor cores), prefill_simt.cuh (fp32 and
+// d = 64: CUDA cores, exact fp32) and the state initialiser below.  Declarations and the
 // contract of every entry point are in include/lizard_attn.h.
 #include <cuda_runtime.h>
 
@@ -13,6 +14,7 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "prefill_simt.cuh"
+#include "prefill_tc.cuh"
 
 namespace lizard {
 
@@ -61,6 +63,58 @@ static lizard_status launch_prefill(const PrefillArgs &pa, cudaStream_t s)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
     kern<<<pa.B * pa.H, SIMT_THREADS, smem, s>>>(pa);
+    return launch_status();
+}
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static encode_tiled_fn tensor_map_encoder()
+{
+    static encode_tiled_fn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<encode_tiled_fn>(p);
+    }
+    return fn;
+}
+
+// [units][L][128] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128B swizzle,
+// rows past L read as zero.
+static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
+{
+    encode_tiled_fn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)L, (cuuint64_t)units};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)L * 128 * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
+{
+    const int units = pa.B * pa.H;
+    CUtensorMap tq, tk, tv;
+    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
+        !make_token_map(&tv, pa.v, units, pa.L))
+        return LIZARD_ERR_CUDA;
+    tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
+                  static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
+                  static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
+                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
+                  (pa.w - 1 + tc::C - 1) / tc::C};
+    if (cudaFuncSetAttribute(tc::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc::SMEM_BYTES) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    tc::prefill_tc_kernel<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
     return launch_status();
 }
 
@@ -133,12 +187,13 @@ lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, c
             return LIZARD_ERR_INVALID_ARG;
     }
     if (B == 0) return LIZARD_OK;
+    if (L == 0) return st ? lizard_state_init(st, stream) : LIZARD_OK;  // the empty prompt leaves the empty state
     PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m,
                    st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
                    st ? st->pos : nullptr};
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == LIZARD_BF16)
-        return dk == 128 ? launch_prefill<__nv_bfloat16, 128>(pa, s) : launch_prefill<__nv_bfloat16, 64>(pa, s);
+        return dk == 128 ? launch_prefill_tc(pa, s) : launch_prefill<__nv_bfloat16, 64>(pa, s);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "lib", "liblizard_attn.so")
 
 LIZARD_OK, LIZARD_ERR_INVALID_ARG, LIZARD_ERR_UNSUPPORTED, LIZARD_ERR_CUDA, LIZARD_ERR_TIMEOUT = range(5)
 LIZARD_F32, LIZARD_BF16 = 0, 1
-LIZARD_MAX_WINDOW = 256
+LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
 EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_decode_step",

@@ -56,7 +56,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *lizard_stream_t;
 
-#define LIZARD_MAX_WINDOW 256
+#define LIZARD_MAX_WINDOW 128
 #define LIZARD_MAX_META 16
 
 typedef enum {

@@ -55,7 +55,7 @@ def _run_decode(wl, steps, seq=None):
     (128, 64, 4, 10, "bf16"),     # ring still filling (pos < w)
     (64, 16, 0, 40, "f32"),       # no sinks
     (64, 1, 3, 5, "f32"),         # window of one token
-    (128, 256, 16, 300, "bf16"),  # largest window and meta count
+    (128, 128, 16, 300, "bf16"),  # largest window and meta count
 ])
 def test_decode_small(d, w, m, hist, dtype):
     wl = WORKLOADS["decode"].replace(B=3, H=4, dk=d, dv=d, w=w, m=m, L=hist, dtype=dtype)

@@ -48,12 +48,20 @@ CASES = [
     ("single_token", "bf16", 2, 2, 1, 128, 16, 4, 3.0, 1.0, 0.5),
     ("no_meta", "f32", 1, 2, 130, 64, 16, 0, 3.0, 1.0, 0.5),
     ("window_one", "f32", 1, 2, 97, 64, 1, 2, 3.0, 1.0, 0.7),
-    ("max_window_max_meta", "bf16", 1, 2, 600, 128, 256, 16, 3.0, 1.0, 1.0),
+    ("max_window_max_meta", "bf16", 1, 2, 600, 128, 128, 16, 3.0, 1.0, 1.0),
     ("strong_decay", "bf16", 1, 4, 512, 128, 128, 8, 0.0, 2.0, 0.5),
     ("very_strong_decay", "f32", 1, 2, 300, 64, 32, 4, -6.0, 3.0, 1.0),
     ("open_gates", "f32", 1, 2, 200, 64, 16, 4, 12.0, 0.5, 1.0),
     ("d64_bf16", "bf16", 2, 3, 257, 64, 64, 4, 3.0, 1.0, 1.0),
     ("more_units_than_sms", "bf16", 5, 32, 70, 128, 64, 4, 3.0, 1.0, 1.0),
+    # tensor-core path edge cases (bf16, d = 128)
+    ("extreme_decay_exact_intra", "bf16", 1, 2, 300, 128, 64, 4, -8.0, 4.0, 1.0),
+    ("mixed_decay", "bf16", 1, 3, 520, 128, 32, 4, -1.0, 3.0, 0.8),
+    ("window_one_bf16", "bf16", 1, 2, 150, 128, 1, 3, 3.0, 1.0, 1.0),
+    ("window_65", "bf16", 1, 2, 333, 128, 65, 4, 3.0, 1.0, 1.0),
+    ("window_66", "bf16", 1, 2, 333, 128, 66, 4, 3.0, 1.0, 1.0),
+    ("one_chunk_exact", "bf16", 2, 2, 64, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("alpha_zero", "bf16", 1, 2, 190, 128, 64, 4, 3.0, 1.0, 0.0),
 ]
 
 
