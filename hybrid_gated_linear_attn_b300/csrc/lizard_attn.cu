@@ -111,10 +111,11 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
                   (pa.w - 1 + tc::C - 1) / tc::C};
-    if (cudaFuncSetAttribute(tc::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc::SMEM_BYTES) != cudaSuccess)
+    auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
+                                                                          : tc::prefill_tc_kernel<2>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    tc::prefill_tc_kernel<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
+    kern<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
     return launch_status();
 }
 

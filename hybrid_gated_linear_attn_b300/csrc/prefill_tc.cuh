@@ -67,7 +67,7 @@ constexpr uint32_t OFF_KL = OFF_KW + 3 * TILE;     // 16 KB: k * e^{b_last - b} 
 constexpr uint32_t OFF_MU = OFF_KL + 2 * TILE;     // 4 KB: meta keys, 16 rows x 128
 constexpr uint32_t MU_BLOCK = META_ROWS * 128;
 constexpr uint32_t OFF_VEC = OFF_MU + 2 * MU_BLOCK;
-constexpr uint32_t VEC_FLOATS = 4 * 128 + 4 * 64;  // xch, first, last, dec, red[2][2][64]
+constexpr uint32_t VEC_FLOATS = 4 * 128 + 3 * 128 + 4 * 64;  // xch[4][128], first, last, dec, red[2][2][64]
 constexpr uint32_t OFF_BAR = OFF_VEC + VEC_FLOATS * 4;
 constexpr uint32_t NBARS = 1 + NR + 3;
 constexpr uint32_t SMEM_USED = OFF_BAR + NBARS * 8 + 16;
@@ -112,15 +112,29 @@ __device__ __forceinline__ uint32_t tmem_lane(uint32_t quarter) { return (32u * 
 __device__ __forceinline__ __nv_bfloat16 ld_bf16(const uint8_t *p) { return *reinterpret_cast<const __nv_bfloat16 *>(p); }
 __device__ __forceinline__ void st_bf16(uint8_t *p, float x) { *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x); }
 
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi)
+{
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// NP = previous chunks in the window band (ceil((w - 1) / 64)).
+template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a)
 {
+    constexpr int NB = NP + 1;     // band chunks
+    constexpr int PART = 16 * NB;  // band columns per softmax thread (four threads per row)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float *xch = reinterpret_cast<float *>(sm + OFF_VEC);
-    float *first2 = xch + 128, *last2 = first2 + 128, *dec = last2 + 128;
+    float *xch = reinterpret_cast<float *>(sm + OFF_VEC);  // [token quarter 4][128]
+    float *first2 = xch + 512, *last2 = first2 + 128, *dec = last2 + 128;
     float *red = dec + 128;  // [pass 2][half 2][row 64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *bar_q = bars, *bar_kv = bars + 1;
@@ -129,9 +143,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int unit = blockIdx.x, h = unit % a.H;
-    const int L = a.L, NP = a.nprev, w = a.w, m = a.m;
+    const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
-    const int gi = tid & 127, gth = tid >> 7;  // prep: key dim and token half
+    // Prep mapping: key dims 2ip and 2ip+1, tokens 16*tqr .. 16*tqr+15.
+    const int ip = tid & 63, tqr = tid >> 6;
+    // Softmax mapping (M = 64 accumulator layout): row srow, column part 2*half + ssub.
+    const int srow = 16 * quarter + (lane & 15), ssub = lane >> 4;
 
     if (warp == 0) {
         tmem_alloc(tmem_slot, T_COLS);
@@ -200,14 +217,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (nchunks > 1) issue_kv(1);
     }
 
-    // Gate logits of this thread's (key dim, 32 tokens), one chunk ahead.
-    const __nv_bfloat16 *gp = a.g + (size_t)unit * L * D + gi;
-    float gnext[32];
+    // Gate logits of this thread's two key dims for its 16 tokens, one chunk
+    // ahead, as packed bf16 pairs (+inf past the end: no decay).
+    const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * D + 2 * ip);
+    uint32_t gnext[16];
     auto load_g = [&](int c) {
 #pragma unroll
-        for (int tt = 0; tt < 32; ++tt) {
-            const int tg = c * C + 32 * gth + tt;
-            gnext[tt] = tg < L ? __bfloat162float(gp[(size_t)tg * D]) : INFINITY;  // past the end: no decay
+        for (int tt = 0; tt < 16; ++tt) {
+            const int tg = c * C + 16 * tqr + tt;
+            gnext[tt] = tg < L ? gp[(size_t)tg * (D / 2)] : 0x7F807F80u;
         }
     };
     if (nchunks > 0) load_g(0);
@@ -233,6 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_bf16_ss(tmem + T_SC, ad, smem_desc(sb + OFF_MU + (kk / 4) * MU_BLOCK + (kk % 4) * 32, 16, 1024),
                             id16, kk > 0);
             }
+#pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
                 if (cj < 0) continue;
@@ -247,60 +266,81 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
 
         // ---- P2: log-space gate prefix sums and the folded operands ----
-        float b2[32];
+        float b2a[16], b2b[16];
         {
-            float run = 0.f;
+            float ra = 0.f, rb = 0.f;
 #pragma unroll
-            for (int tt = 0; tt < 32; ++tt) {
-                run += log2_sigmoid(gnext[tt]);
-                b2[tt] = run;
+            for (int tt = 0; tt < 16; ++tt) {
+                const float2 gg = bf2_to_f2(gnext[tt]);
+                ra += log2_sigmoid(gg.x);
+                rb += log2_sigmoid(gg.y);
+                b2a[tt] = ra;
+                b2b[tt] = rb;
             }
-            if (gth == 0) {
-                xch[gi] = run;
-                first2[gi] = b2[0];
+            xch[tqr * 128 + 2 * ip] = ra;
+            xch[tqr * 128 + 2 * ip + 1] = rb;
+            if (tqr == 0) {
+                first2[2 * ip] = b2a[0];
+                first2[2 * ip + 1] = b2b[0];
             }
         }
         __syncthreads();
-        if (gth == 1) {
-            const float off = xch[gi];
+        {
+            float oa = 0.f, ob = 0.f;
+            for (int qq = 0; qq < tqr; ++qq) {
+                oa += xch[qq * 128 + 2 * ip];
+                ob += xch[qq * 128 + 2 * ip + 1];
+            }
 #pragma unroll
-            for (int tt = 0; tt < 32; ++tt) b2[tt] += off;
+            for (int tt = 0; tt < 16; ++tt) {
+                b2a[tt] += oa;
+                b2b[tt] += ob;
+                if (16 * tqr + tt == n - 1) {
+                    last2[2 * ip] = b2a[tt];
+                    last2[2 * ip + 1] = b2b[tt];
+                }
+            }
         }
-#pragma unroll
-        for (int tt = 0; tt < 32; ++tt)
-            if (32 * gth + tt == n - 1) last2[gi] = b2[tt];
         __syncthreads();
-        const float f2 = first2[gi], l2 = last2[gi];
-        const float span = f2 - l2;
-        const int unsafe = __syncthreads_or(span > SPAN_MAX2);
-        if (gth == 0) dec[gi] = ex2(l2);
+        const float f2a = first2[2 * ip], l2a = last2[2 * ip];
+        const float f2b = first2[2 * ip + 1], l2b = last2[2 * ip + 1];
+        const int unsafe = __syncthreads_or(f2a - l2a > SPAN_MAX2 || f2b - l2b > SPAN_MAX2);
+        if (tqr == 0) {
+            dec[2 * ip] = ex2(l2a);
+            dec[2 * ip + 1] = ex2(l2b);
+        }
         if (c + 1 < nchunks) load_g(c + 1);
 
-        float q0[32];
+        float q0a[16], q0b[16];
         {
-            const float r2 = 0.5f * (f2 + l2);
-            const float E = ex2(r2), F = ex2(-0.5f * span);
-            const uint32_t blk = (gi / 64) * TILE, byte = (gi % 64) * 2;
-#pragma unroll 4
-            for (int tt = 0; tt < 32; ++tt) {
-                const int t = 32 * gth + tt;
+            const float r2a = 0.5f * (f2a + l2a), r2b = 0.5f * (f2b + l2b);
+            const float Ea = ex2(r2a), Eb = ex2(r2b);
+            const float Fa = ex2(0.5f * (l2a - f2a)), Fb = ex2(0.5f * (l2b - f2b));
+            const uint32_t blk = (ip / 32) * TILE, byte = (ip % 32) * 4;
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt) {
+                const int t = 16 * tqr + tt;
                 const uint32_t o = blk + sw128_offset(t, byte);
-                const float qv = __bfloat162float(ld_bf16(sm + OFF_Q + o));
-                const float kv = __bfloat162float(ld_bf16(sm + slot_off + o));
-                float kl;
+                const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_Q + o));
+                const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + slot_off + o));
+                float kla, klb;
                 if (!unsafe) {
-                    const float e = ex2(b2[tt] - r2), ie = ex2(r2 - b2[tt]);
-                    const float qr = qv * e, kr = kv * ie;
-                    st_bf16(sm + OFF_QZ + o, qr);
-                    st_bf16(sm + OFF_KW + o, kr);
-                    q0[tt] = qr * E;
-                    kl = kr * F;
+                    const float qra = qv.x * ex2(b2a[tt] - r2a), qrb = qv.y * ex2(b2b[tt] - r2b);
+                    const float kra = kv.x * ex2(r2a - b2a[tt]), krb = kv.y * ex2(r2b - b2b[tt]);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_QZ + o) = f2_to_bf2(qra, qrb);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_KW + o) = f2_to_bf2(kra, krb);
+                    q0a[tt] = qra * Ea;
+                    q0b[tt] = qrb * Eb;
+                    kla = kra * Fa;
+                    klb = krb * Fb;
                 } else {
-                    reinterpret_cast<float *>(sm + OFF_QZ)[t * D + gi] = b2[tt];
-                    q0[tt] = qv * ex2(b2[tt]);
-                    kl = kv * ex2(l2 - b2[tt]);
+                    *reinterpret_cast<float2 *>(sm + OFF_QZ + ((size_t)t * D + 2 * ip) * 4) = make_float2(b2a[tt], b2b[tt]);
+                    q0a[tt] = qv.x * ex2(b2a[tt]);
+                    q0b[tt] = qv.y * ex2(b2b[tt]);
+                    kla = kv.x * ex2(l2a - b2a[tt]);
+                    klb = kv.y * ex2(l2b - b2b[tt]);
                 }
-                st_bf16(sm + OFF_KL + o, kl);
+                *reinterpret_cast<uint32_t *>(sm + OFF_KL + o) = f2_to_bf2(kla, klb);
             }
         }
         fence_proxy_async_smem();
@@ -325,10 +365,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (__syncthreads_or(!ok)) { aborted = true; break; }
         tc_fence_after();
         if (unsafe) {
-            // Exact A[t][s] = sum_i q_ti k_si 2^{b2_ti - b2_si}, s <= t, on the CUDA cores.
-            // Row t = 16*quarter + (lane & 15); lanes >= 16 take the second 16 of the warp's 32 columns.
-            const int t = 16 * quarter + (lane & 15);
-            const int s0 = 32 * half + 16 * (lane >> 4);
+            // Exact A[t][s] = sum_i q_ti k_si 2^{b2_ti - b2_si} for s <= t on
+            // the CUDA cores; this thread's row srow, columns 16p .. 16p+15.
+            const int t = srow, s0 = 16 * (2 * half + ssub);
             const float *bz = reinterpret_cast<const float *>(sm + OFF_QZ);
             float acc[16];
 #pragma unroll
@@ -346,112 +385,114 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // lanes 16..31 hand their 16 columns to lanes 0..15, which own the TMEM rows
-            uint32_t lo[16], hi[16];
+            uint32_t r[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float other = __shfl_down_sync(0xffffffffu, acc[e], 16);
-                lo[e] = __float_as_uint(acc[e]);
-                hi[e] = __float_as_uint(other);
-            }
-            tmem_st16(tmem + tmem_lane(quarter) + T_A + 32 * half, lo);
-            tmem_st16(tmem + tmem_lane(quarter) + T_A + 32 * half + 16, hi);
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(acc[e]);
+            tmem_st16_x2<16>(tmem + tmem_lane(quarter) + T_A + 32 * half, r);
             tmem_wait_st();
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
         }
 
-        // ---- P4: next q tile; q*e^{b} operand; window softmax with sinks -> W ----
+        // ---- P4: next q tile; q*e^{b} operand and y^T part 1; softmax -> W ----
         if (tid == 0 && c + 1 < nchunks) {
             fence_proxy_async_smem();
             issue_q(c + 1);
         }
         {
-            const uint32_t blk = (gi / 32) * TILE, byte = (gi % 32) * 4;
+            const uint32_t blk = (ip / 16) * TILE, byte = (ip % 16) * 8;
 #pragma unroll
-            for (int tt = 0; tt < 32; ++tt)
-                *reinterpret_cast<float *>(sm + OFF_QZ + blk + sw128_offset(32 * gth + tt, byte)) = q0[tt];
+            for (int tt = 0; tt < 16; ++tt)
+                *reinterpret_cast<float2 *>(sm + OFF_QZ + blk + sw128_offset(16 * tqr + tt, byte)) =
+                    make_float2(q0a[tt], q0b[tt]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {  // y^T part 1 = S^T (q e^{b})^T, overlapping the softmax below
+            const uint32_t idt = instr_desc(128, 64, FMT_TF32, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                const uint64_t bd = smem_desc(sb + OFF_QZ + (kk / 4) * TILE + (kk % 4) * 32, 16, 1024);
+                mma_tf32_ts(tmem + T_Y1, tmem + T_ST + kk * 8, bd, idt, kk > 0);
+            }
         }
         {
-            const int t = 16 * quarter + (lane & 15);
-            const bool own = lane < 16;
-            const bool rowok = own && t < n;
-            const int tg = c0 + t;
-            const int nb = NP + 1;
-            const int cbeg = half * 32 * nb, cend = cbeg + 32 * nb;   // this half's band columns
-            const int pbase = c0 - 64 * NP;                           // global position of band column 0
+            const int t = srow, tg = c0 + t, p = 2 * half + ssub;
+            const bool rowok = t < n;
+            const int pbase = c0 - 64 * NP;  // global position of band column 0
             const uint32_t tl = tmem + tmem_lane(quarter);
+            uint32_t rr[NB][16], rm[16];
+#pragma unroll
+            for (int gq = 0; gq < NB; ++gq) tmem_ld16_x2<PART>(tl + T_SC + 16 + 2 * PART * half + 16 * gq, rr[gq]);
+            tmem_ld16_x2<PART>(tl + T_SC, rm);
+            tmem_wait_ld();
+            const bool meta_owner = half == 0 && ssub == 0;
+            float x[PART];
             float mx = -INFINITY;
-            uint32_t r[16];
-            if (half == 0) {
-                tmem_ld16(tl + T_SC, r);
-                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < META_ROWS; ++j)
-                    if (j < m) mx = fmaxf(mx, __uint_as_float(r[j]));
-            }
-            for (int cc = cbeg; cc < cend; cc += 16) {
-                tmem_ld16(tl + T_SC + 16 + cc, r);
-                tmem_wait_ld();
+            for (int gq = 0; gq < NB; ++gq)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int p = pbase + cc + e;
-                    if (p >= 0 && p <= tg && p > tg - w) mx = fmaxf(mx, __uint_as_float(r[e]));
+                    const int pp = pbase + PART * p + 16 * gq + e;
+                    const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
+                    x[16 * gq + e] = valid ? __uint_as_float(rr[gq][e]) : -INFINITY;
+                    mx = fmaxf(mx, x[16 * gq + e]);
                 }
+            if (meta_owner) {
+#pragma unroll
+                for (int j = 0; j < META_ROWS; ++j)
+                    if (j < m) mx = fmaxf(mx, __uint_as_float(rm[j]));
             }
-            if (own) red[half * 64 + t] = mx;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            if (ssub == 0) red[half * 64 + t] = mx;
             __syncthreads();
-            const float M = fmaxf(red[t], red[64 + t]);
-            const float M2 = M * LOG2E;
+            const float M2 = fmaxf(red[t], red[64 + t]) * LOG2E;
             float sum = 0.f;
-            if (half == 0) {
-                tmem_ld16(tl + T_SC, r);
-                tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < PART; ++k) {
+                x[k] = ex2(x[k] * LOG2E - M2);
+                sum += x[k];
+            }
+            if (meta_owner) {
 #pragma unroll
                 for (int j = 0; j < META_ROWS; ++j)
-                    if (j < m) sum += ex2(__uint_as_float(r[j]) * LOG2E - M2);
+                    if (j < m) sum += ex2(__uint_as_float(rm[j]) * LOG2E - M2);
             }
-            for (int cc = cbeg; cc < cend; cc += 16) {
-                tmem_ld16(tl + T_SC + 16 + cc, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int p = pbase + cc + e;
-                    if (p >= 0 && p <= tg && p > tg - w) sum += ex2(__uint_as_float(r[e]) * LOG2E - M2);
-                }
-            }
-            if (own) red[128 + half * 64 + t] = sum;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+            if (ssub == 0) red[128 + half * 64 + t] = sum;
             __syncthreads();
             const float inv = a.alpha / (red[128 + t] + red[192 + t]);
-            for (int cc = cbeg; cc < cend; cc += 16) {
-                tmem_ld16(tl + T_SC + 16 + cc, r);
+#pragma unroll
+            for (int gq = 0; gq < NB; ++gq) {
+                const int colw = 2 * PART * half + 16 * gq;  // band column of lanes 0..15 (lanes 16..31: + PART)
+                const int col0 = colw + PART * ssub;         // this thread's 16 band columns start here
                 uint32_t ra[16];
-                const int s0 = cc - 64 * NP;  // column within this chunk (A), when >= 0
-                if (s0 >= 0) tmem_ld16(tl + T_A + s0, ra);
-                tmem_wait_ld();
+                const bool need_a = colw + PART + 16 > 64 * NP;  // some lane reaches the current chunk
+                if (need_a) {
+                    tmem_ld16_x2<PART>(tl + T_A + colw - 64 * NP, ra);
+                    tmem_wait_ld();
+                }
                 uint32_t packed[8];
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
                     float wv[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int p = pbase + cc + e + u;
-                        float x = 0.f;
-                        if (p >= 0 && p <= tg && p > tg - w) x = ex2(__uint_as_float(r[e + u]) * LOG2E - M2) * inv;
-                        if (s0 >= 0 && p <= tg) x += __uint_as_float(ra[e + u]);
-                        wv[u] = rowok ? x : 0.f;
+                        const int col = col0 + e + u, s = col - 64 * NP;
+                        float v = x[16 * gq + e + u] * inv;
+                        if (need_a && s >= 0 && pbase + col <= tg) v += __uint_as_float(ra[e + u]);
+                        wv[u] = rowok ? v : 0.f;
                     }
-                    __nv_bfloat162 pr = __floats2bfloat162_rn(wv[0], wv[1]);
-                    packed[e / 2] = *reinterpret_cast<uint32_t *>(&pr);
+                    packed[e / 2] = f2_to_bf2(wv[0], wv[1]);
                 }
-                if (own) {
-                    const uint32_t blk = (cc / 64) * TILE, byte = (cc % 64) * 2;
-                    *reinterpret_cast<uint4 *>(sm + OFF_KW + blk + sw128_offset(t, byte)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_KW + blk + sw128_offset(t, byte + 16)) =
-                        make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                }
+                const uint32_t blk = (col0 / 64) * TILE, byte = (col0 % 64) * 2;
+                *reinterpret_cast<uint4 *>(sm + OFF_KW + blk + sw128_offset(t, byte)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_KW + blk + sw128_offset(t, byte + 16)) =
+                    make_uint4(packed[4], packed[5], packed[6], packed[7]);
             }
         }
         fence_proxy_async_smem();
@@ -459,16 +500,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncthreads();
         tc_fence_after();
 
-        // ---- P5: y^T = S^T (q e^{b})^T + V_band^T W^T ----
+        // ---- P5: y^T part 2 = V_band^T W^T ----
         if (tid == 0) {
-            const uint32_t idt = instr_desc(128, 64, FMT_TF32, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t bd = smem_desc(sb + OFF_QZ + (kk / 4) * TILE + (kk % 4) * 32, 16, 1024);
-                mma_tf32_ts(tmem + T_Y1, tmem + T_ST + kk * 8, bd, idt, kk > 0);
-            }
             const uint32_t idv = instr_desc(128, 64, FMT_BF16, 1, 0);
             bool first = true;
+#pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
                 if (cj < 0) continue;
@@ -494,18 +530,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (warp < 4) {
             const uint32_t tl = tmem + tmem_lane(quarter) + T_ST;
-            for (int cc = 0; cc < D; cc += 16) {
-                uint32_t r[16];
-                tmem_ld16(tl + cc, r);
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tl + cc, r0);
+                tmem_ld16(tl + cc + 16, r1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * dec[cc + e]);
-                tmem_st16(tl + cc, r);
+                for (int e = 0; e < 16; ++e) {
+                    r0[e] = __float_as_uint(__uint_as_float(r0[e]) * dec[cc + e]);
+                    r1[e] = __float_as_uint(__uint_as_float(r1[e]) * dec[cc + 16 + e]);
+                }
+                tmem_st16(tl + cc, r0);
+                tmem_st16(tl + cc + 16, r1);
             }
             tmem_wait_st();
         } else {
             const int j = 32 * quarter + lane;
             __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
+#pragma unroll
             for (int cc = 0; cc < C; cc += 16) {
                 uint32_t r1[16], r2[16];
                 tmem_ld16(tmem + tmem_lane(quarter) + T_Y1 + cc, r1);
@@ -513,7 +556,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    if (cc + e < n) yp[(size_t)(cc + e) * D] = __float2bfloat16_rn(__uint_as_float(r1[e]) + __uint_as_float(r2[e]));
+                    if (cc + e < n)
+                        yp[(size_t)(cc + e) * D] = __float2bfloat16_rn(__uint_as_float(r1[e]) + __uint_as_float(r2[e]));
             }
         }
         tc_fence_before();

@@ -21,8 +21,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Byte offset of element `col` (elements of `esize` bytes) of row `row` in a
-// 128B-swizzled tile whose rows are 128 B.
+// Byte offset of byte `byte_in_row` of row `row` in a 128B-swizzled tile
+// whose rows are 128 B (tile base 1024-byte aligned).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row)
 {
     return row * 128u + ((((byte_in_row >> 4) ^ (row & 7u)) << 4) | (byte_in_row & 15u));
@@ -121,6 +121,30 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
                  : "memory")
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) { LZ_TMEM_LD16(taddr, r); }
+
+// 16 lanes x 32-bit in two halves: threads 0..15 read lanes 0..15 of the
+// warp's quarter at columns [c, c+16); threads 16..31 read the same lanes at
+// columns [c+OFF, c+OFF+16).  Suits the M = 64 accumulator layout, whose rows
+// occupy lanes 0..15 of each quarter.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld16_x2(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+                 " [%16], %17;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr), "n"(OFF));
+}
+template <int OFF>
+__device__ __forceinline__ void tmem_st16_x2(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                 "%15,%16,%17};" ::"r"(taddr),
+                 "n"(OFF), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) { LZ_TMEM_ST16(taddr, r); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
