@@ -35,7 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from hybrid_gated_linear_attn_b300.inputs import (WORKLOADS, decode_initial_state,  # noqa: E402
-                                                  decode_step_inputs, prefill_inputs)
+                                                  decode_step_inputs, prefill_inputs, torch_dtype)
 
 METRIC = "prefill tokens/s & % bf16 TC roofline; decode tokens/s & HBM GB/s (1 B300)"
 PREFILL_WL = WORKLOADS["llama3_8b"]
@@ -394,6 +394,37 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_profile_case(args):
+    """Launch one operator of one workload W + K times and print nothing else:
+    the program that ncu captures on a small case.  ``--batch`` overrides the
+    workload's batch (sequences)."""
+    from hybrid_gated_linear_attn_b300 import LizardState, lizard_attn_decode_step, lizard_attn_prefill
+    from hybrid_gated_linear_attn_b300 import lizard_check_device_status
+
+    wl = WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(B=args.batch)
+    if args.profile_case == "prefill":
+        inp = prefill_inputs(wl)
+        q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
+        y = torch.empty_like(v)
+        st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
+        fn = lambda: lizard_attn_prefill(q, k, v, g, mu, wl.alpha, wl.w, y=y, state=st)  # noqa: E731
+    else:
+        init = decode_initial_state(wl)
+        st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=torch_dtype(wl.dtype))
+        for n in ("S", "ring_k", "ring_v", "pos"):
+            getattr(st, n).copy_(init[n])
+        mu = init["mu"].cuda()
+        p = {n: t.cuda() for n, t in decode_step_inputs(wl, 0).items()}
+        fn = lambda: lizard_attn_decode_step(p["q"], p["k"], p["v"], p["g"], mu, wl.alpha, st)  # noqa: E731
+    for _ in range(args.warmup + args.steps):
+        fn()
+    lizard_check_device_status()
+    torch.cuda.synchronize()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,8 +434,16 @@ def main(argv=None):
     ap.add_argument("--sample-heads", type=int, default=None,
                     help="(batch, head) units in the oracle's timed sample (default: the whole workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+                    help="only launch this operator W + K times (a small program for ncu); no JSON line")
+    ap.add_argument("--workload", default=None, help="workload of --profile-case (default: the bench's)")
+    ap.add_argument("--batch", type=int, default=0, help="batch override for --profile-case")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
+    if args.profile_case:
+        if args.workload is None:
+            args.workload = "llama3_8b" if args.profile_case == "prefill" else "decode"
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     if world > 1:
