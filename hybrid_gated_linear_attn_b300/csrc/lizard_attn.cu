@@ -119,17 +119,26 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
     return launch_status();
 }
 
+static int sm_count()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 1;
+    }
+    return n;
+}
+
 template <typename T, int D>
 static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
 {
-    const size_t smem = decode_smem_bytes<D>(da.w, da.m);
+    const DecodePlan plan = decode_plan<D>((int)sizeof(T), da.w, da.m);
+    if (plan.total > DECODE_SMEM_MAX) return LIZARD_ERR_UNSUPPORTED;
     auto kern = decode_step_kernel<T, D>;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.total) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<da.B * da.H, DECODE_THREADS, smem, s>>>(da);
-    if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
-    advance_pos_kernel<<<(da.B + 255) / 256, 256, 0, s>>>(const_cast<int64_t *>(da.pos), da.B);
+    kern<<<da.B * da.H * DECODE_SPLIT, DECODE_THREADS, plan.total, s>>>(da);
     return launch_status();
 }
 

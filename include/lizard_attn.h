@@ -123,7 +123,12 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
  * At p = pos[b]: S <- diag(sigmoid(g)) S + k^T v; yg = q S; the window is the
  * current token plus tokens max(0, p-w+1) .. p-1 read from the ring; then
  * the current k, v go to ring slot p % w and pos[b] becomes p + 1.
- * Enqueues two kernels (the step, then the pos advance).
+ * Enqueues one kernel.  Precondition: 0 <= pos[b] < 2^40 (a state written
+ * by this library always is).  While the kernel runs, pos[b] carries an
+ * arrival count in its high bits; it holds p + 1 again once the step is
+ * done.  A pos outside that range is reported (see
+ * lizard_check_device_status); that sequence's y, S, ring and pos are then
+ * undefined, but every access stays inside the caller's buffers.
  */
 LIZARD_API lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g,
                                       const void *meta_k, float alpha, int m, void *y,
@@ -133,8 +138,7 @@ LIZARD_API lizard_status lizard_attn_decode_step(const void *q, const void *k, c
  * lizard_check_device_status: synchronises `stream`, then reads and clears
  * the library's device error word.  LIZARD_ERR_TIMEOUT if a kernel since the
  * last check abandoned a bounded wait (its outputs are then undefined),
- * LIZARD_ERR_INVALID_ARG if a decode step found a negative pos (that
- * sequence's outputs and state were left untouched), LIZARD_ERR_CUDA if
+ * LIZARD_ERR_INVALID_ARG if a decode step found a pos outside [0, 2^40), LIZARD_ERR_CUDA if
  * synchronising failed, LIZARD_OK otherwise.
  */
 LIZARD_API lizard_status lizard_check_device_status(lizard_stream_t stream);

@@ -99,3 +99,30 @@ def test_prefill_then_decode_equals_longer_prefill(L, w, n):
         y = gpu_decode_step(step, inp["mu"], inp["alpha"], st).cpu()
         err = rel_l2(y, y_ref[:, :, t])
         assert err <= 1e-2, f"t={t}: rel L2 {err:.3e}"
+
+
+def test_decode_reports_a_position_outside_the_valid_range():
+    """A pos outside [0, 2^40) is reported by lizard_check_device_status;
+    the other sequences of the same call are still exact and every pos of a
+    valid sequence advances by one."""
+    from hybrid_gated_linear_attn_b300 import LizardError, lizard_check_device_status
+    from hybrid_gated_linear_attn_b300.lizard_attn import LIZARD_ERR_INVALID_ARG
+
+    wl = WORKLOADS["decode"].replace(B=3, H=4, L=20)
+    init = decode_initial_state(wl)
+    st = _gpu_state_from(init, wl)
+    st.pos[1] = -5
+    inp = decode_step_inputs(wl, 0)
+    y = gpu_decode_step(inp, init["mu"], wl.alpha, st).cpu()
+    with pytest.raises(LizardError) as e:
+        lizard_check_device_status()
+    assert e.value.status == LIZARD_ERR_INVALID_ARG
+    lizard_check_device_status()  # the error word was cleared
+    seq = [0, 2]
+    ost = dict(S=init["S"][seq].double().contiguous(), ring_k=init["ring_k"][seq].contiguous(),
+               ring_v=init["ring_v"][seq].contiguous(), pos=init["pos"][seq].clone())
+    sub = {n: inp[n][seq].contiguous() for n in ("q", "k", "v", "g")}
+    y_ref = O.decode_step(sub["q"], sub["k"], sub["v"], sub["g"], init["mu"], wl.alpha, ost)
+    assert rel_l2(y[seq], y_ref) <= 1e-2
+    pos = st.pos.cpu()
+    assert int(pos[0]) == wl.L + 1 and int(pos[2]) == wl.L + 1
