@@ -15,6 +15,7 @@
 #include "decode.cuh"
 #include "prefill_simt.cuh"
 #include "prefill_tc.cuh"
+#include "prefill_ws.cuh"
 
 namespace lizard {
 
@@ -130,6 +131,34 @@ static int sm_count()
     return n;
 }
 
+template <int NP>
+static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                          const ws::WsArgs &wa, int units, cudaStream_t s)
+{
+    auto kern = ws::prefill_ws_kernel<NP>;
+    constexpr uint32_t smem = ws::Smem<NP>::BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    kern<<<units, ws::THREADS, smem, s>>>(tq, tk, tv, wa);
+    return launch_status();
+}
+
+// Warp-specialised tensor-core prefill (bf16, d = 128, w <= 65).
+static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s)
+{
+    const int units = pa.B * pa.H;
+    CUtensorMap tq, tk, tv;
+    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
+        !make_token_map(&tv, pa.v, units, pa.L))
+        return LIZARD_ERR_CUDA;
+    ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
+                  static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
+                  static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
+                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m};
+    return pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, wa, units, s)
+                     : launch_prefill_ws_np<1>(tq, tk, tv, wa, units, s);
+}
+
 template <typename T, int D>
 static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
 {
@@ -203,7 +232,8 @@ lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, c
                    st ? st->pos : nullptr};
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == LIZARD_BF16)
-        return dk == 128 ? launch_prefill_tc(pa, s) : launch_prefill<__nv_bfloat16, 64>(pa, s);
+        return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
+                         : launch_prefill<__nv_bfloat16, 64>(pa, s);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 

@@ -1,0 +1,718 @@
+// prefill_ws.cuh -- chunked Lizard prefill on tcgen05 tensor cores as a
+// warp-specialised pipeline (bf16 inputs, d = 128, window w <= 65).
+//
+// Operator: gated linear attention (Lizard, gist.science/de section 2 item 1)
+// + anchor window with meta-memory sinks (item 2) + alpha combine (item 3).
+// The chunked, log-space form follows the page's "Hardware-bewusster
+// Algorithmus" section: cumulative gate terms are kept as log-space prefix
+// sums and folded into the query/key operands, so the intra-chunk work is
+// plain GEMMs on the tensor cores.
+//
+// One CTA walks the chunks (C = 64 tokens) of one (batch, head) sequence.
+// Per chunk c (tokens c0 .. c0+63), with b_t = sum_{r=c0..t} log2 sigmoid(g_r)
+// per key dim (fp32, base 2) and the reference r = b_{c0+31} (the end of the
+// first half of the chunk):
+//
+//   SC  [t, s'] = q_t . k_s'  over the band (previous chunk, this chunk)
+//                 and q_t . mu_j                              tcgen05, M=64
+//   A   [t, s]  = QR_t . KR_s,  QR = q 2^{b-r}, KR = k 2^{r-b}  tcgen05, M=64
+//   W   [t, s'] = alpha softmax-with-sinks(SC)[t, s'] + A[t, s] (s <= t)
+//   Y^T [j, t]  = S16 QR^T + V_band^T W^T                       tcgen05, M=128
+//                 (S16 = bf16(S^T diag(2^r)) in tensor memory: q 2^{b} S)
+//   S^T        <- S^T diag(2^{b_last}) + V^T KL,  KL = k 2^{b_last - b}
+//
+// The factors of A have exponents within +-(half-chunk decay span); a chunk
+// whose half-span exceeds SPAN2_MAX (base 2) for some key dimension is
+// "unsafe": its A is computed exactly on the CUDA cores instead
+// (sum_i q k 2^{b_t - b_s}, exponent <= 0), and its QR uses r = 0.  So every
+// gate value is handled.
+//
+// Warp roles (18 warps):
+//   warp 0       TMA producer: q tiles (2 stages), k/v tiles (ring of NP+2)
+//   warp 1       MMA issuer (one thread): all tcgen05.mma, commits
+//   warps 2-5    state pass (S^T decay, S16) and y epilogue; the final state
+//   warps 6-13   gate prep: log-sigmoid, prefix sums, QR / KR / KL operands
+//   warps 14-17  window softmax: W from SC and A
+// Every hand-off is an mbarrier; every wait is bounded (a timeout records
+// DEV_TIMEOUT, drains the copies and products in flight, and returns).
+#pragma once
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace lizard {
+namespace ws {
+
+using namespace sm100;
+
+constexpr int C = 64;
+constexpr int D = 128;
+constexpr int NWARPS = 18;
+constexpr int THREADS = NWARPS * 32;
+constexpr int W_TMA = 0, W_MMA = 1, W_EPI = 2, W_PREP = 6, W_SOFT = 14;
+constexpr int EPI_N = 128, PREP_N = 256, SOFT_N = 128;
+enum : int { NB_EPI = 1, NB_PREP = 2, NB_SOFT = 3, NB_EPI_R = 4, NB_PREP_R = 5, NB_SOFT_R = 6 };
+constexpr int META_ROWS = 16;
+constexpr int KROWS = C + META_ROWS;       // key tile rows: 64 tokens, then the meta keys
+constexpr int QS = 2;                      // q stages
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float SPAN2_MAX = 100.f;         // half-chunk decay span limit (base 2) of the GEMM path
+constexpr uint32_t WAIT_LIMIT = 1u << 21;
+
+// Shared memory (offsets from a 1024-aligned base).
+constexpr uint32_t KB_K = KROWS * 128;     // one 64-dim block of a key tile (80 rows)
+constexpr uint32_t KB_T = C * 128;         // one 64-dim block of a 64-row tile
+constexpr uint32_t SLOT = 2 * KB_K + 2 * KB_T;
+constexpr uint32_t SLOT_V = 2 * KB_K;      // v tile within a slot
+template <int NP>
+struct Smem {
+    static constexpr int NR = NP + 2;
+    static constexpr uint32_t KV = 0;
+    static constexpr uint32_t Q = KV + NR * SLOT;
+    static constexpr uint32_t QR = Q + QS * 2 * KB_T;
+    static constexpr uint32_t KR = QR + 2 * KB_T;
+    static constexpr uint32_t KL = KR + 2 * KB_T;
+    static constexpr uint32_t W = KL + 2 * KB_T;           // KL and W: 32 KB of exact-A scratch
+    static constexpr uint32_t W_BYTES = (NP + 1) * KB_T > 2 * KB_T ? (NP + 1) * KB_T : 2 * KB_T;
+    static constexpr uint32_t VEC = W + W_BYTES;           // dec[2][128], er[2][128], tot[4][128] (fp32)
+    static constexpr uint32_t FLAG = VEC + (2 * 128 + 2 * 128 + 4 * 128) * 4;  // unsafe[2], abort
+    static constexpr uint32_t BAR = FLAG + 16;
+    static constexpr int NBAR = 2 * QS + 2 * NR + 14;
+    static constexpr uint32_t TSLOT = BAR + NBAR * 8;
+    static constexpr uint32_t USED = TSLOT + 16;
+    static constexpr uint32_t BYTES = USED + 1024;
+};
+
+// Tensor-memory columns (512 allocated).
+constexpr uint32_t T_S = 0, T_S16 = 128, T_Y = 192, T_SC = 256;
+template <int NP>
+struct Tmem {
+    static constexpr uint32_t SC_COLS = 64 * NP + 64 + META_ROWS;
+    static constexpr uint32_t A = T_SC + SC_COLS;
+    static_assert(A + 64 <= 512, "tensor memory budget");
+};
+
+struct WsArgs {
+    const __nv_bfloat16 *g, *mu, *k, *v;
+    __nv_bfloat16 *y;
+    float *S_out;
+    __nv_bfloat16 *ring_k, *ring_v;
+    int64_t *pos;
+    float alpha;
+    int H, L, w, m;
+};
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// 2^x on the FMA pipe: x = n + f with f in [0, 1); 2^f by a degree-4
+// least-squares polynomial (relative error < 4e-6), 2^n by exponent
+// arithmetic.  Returns 0 below 2^-126.
+__device__ __forceinline__ float exp2_fma(float x)
+{
+    x = fmaxf(x, -127.f);
+    const float n = floorf(x);
+    const float f = x - n;
+    float p = 0.013683983f;
+    p = fmaf(p, f, 0.051717736f);
+    p = fmaf(p, f, 0.24162132f);
+    p = fmaf(p, f, 0.69296956f);
+    p = fmaf(p, f, 1.0000036f);
+    const int e = (int)n;
+    return e < -126 ? 0.f : __int_as_float(__float_as_int(p) + (e << 23));
+}
+// log2(sigmoid(g)) = min(g, 0) log2(e) - log2(1 + u),  u = 2^{-|g| log2(e)} in (0, 1];
+// log2(1 + u) = u P(u) with a degree-7 least-squares polynomial (absolute
+// error < 4e-7, exactly 0 at u = 0 so open gates give no decay).
+__device__ __forceinline__ float log2_sigmoid(float g)
+{
+    const float u = ex2(-fabsf(g) * LOG2E);
+    float p = 0.015127916f;
+    p = fmaf(p, u, -0.078158207f);
+    p = fmaf(p, u, 0.19238505f);
+    p = fmaf(p, u, -0.32461637f);
+    p = fmaf(p, u, 0.47311336f);
+    p = fmaf(p, u, -0.72051549f);
+    p = fmaf(p, u, 1.4426640f);
+    return fminf(g, 0.f) * LOG2E - u * p;
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi)
+{
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t tlane(uint32_t quarter) { return (32u * quarter) << 16; }
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+// Bounded wait on phase `use` (its parity) of an mbarrier; false on timeout
+// or when another role already gave up.
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int *abort_flag)
+{
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, use & 1u)) return true;
+        if ((i & 255u) == 255u && *abort_flag) return false;
+    }
+    return false;
+}
+
+template <int NP>
+__global__ void __launch_bounds__(THREADS, 1)
+    prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const WsArgs a)
+{
+    using SM = Smem<NP>;
+    using TM = Tmem<NP>;
+    constexpr int NR = SM::NR;
+    constexpr int NB = NP + 1;  // band chunks
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float *dec_v = reinterpret_cast<float *>(sm + SM::VEC);   // [2][128] 2^{b_last}
+    float *er_v = dec_v + 256;                                  // [2][128] 2^{r}
+    float *tot = er_v + 256;                                    // [4][128] quarter totals
+    volatile int *unsafe_f = reinterpret_cast<volatile int *>(sm + SM::FLAG);  // [2]
+    volatile int *abort_f = unsafe_f + 2;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::BAR);
+    uint64_t *q_full = bars, *q_empty = bars + QS, *kv_full = bars + 2 * QS, *kv_empty = kv_full + NR;
+    uint64_t *prep_ready = kv_empty + NR, *kr_free = prep_ready + 1, *qr_free = prep_ready + 2,
+             *kl_free = prep_ready + 3, *sc_full = prep_ready + 4, *a_full = prep_ready + 5,
+             *sc_free = prep_ready + 6, *w_full = prep_ready + 7, *w_free = prep_ready + 8,
+             *s_ready = prep_ready + 9, *st_done = prep_ready + 10, *y_full = prep_ready + 11,
+             *y_free = prep_ready + 12, *drain = prep_ready + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM::TSLOT);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x, h = unit % a.H;
+    const int L = a.L, w = a.w, m = a.m;
+    const int nchunks = (L + C - 1) / C;
+
+    // ---------------------------------------------------------- set-up
+    if (warp == W_MMA) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 2);
+        }
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 14; ++i) mbar_init(&prep_ready[i], i == 5 ? 2 : 1);  // a_full: MMA + prep
+        unsafe_f[0] = 0;
+        unsafe_f[1] = 0;
+        *abort_f = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    // Meta keys of this head into rows 64..79 of every key tile (zero past m).
+    for (int e = tid; e < NR * META_ROWS * 64; e += THREADS) {
+        const int s = e / (META_ROWS * 64), rem = e % (META_ROWS * 64), r = rem / 64, ip = rem % 64;
+        const int i = 2 * ip;
+        uint32_t val = 0u;
+        if (r < m) val = *reinterpret_cast<const uint32_t *>(a.mu + ((size_t)h * m + r) * D + i);
+        *reinterpret_cast<uint32_t *>(sm + SM::KV + s * SLOT + (i / 64) * KB_K +
+                                      sw128_offset(C + r, (i % 64) * 2)) = val;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    bool failed = false;
+    auto give_up = [&]() {
+        failed = true;
+        *abort_f = 1;
+        atomicExch(&g_device_error, DEV_TIMEOUT);
+    };
+
+    if (warp == W_TMA) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_issued[NR] = {}, q_issued[QS] = {};
+            for (int c = 0; c < nchunks && !failed; ++c) {
+                const int s = c % NR;
+                if (c >= NR && !bwait(&kv_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
+                uint8_t *base = sm + SM::KV + s * SLOT;
+                mbar_arrive_expect_tx(&kv_full[s], 2 * KB_T + 2 * KB_T);
+                tma_load_3d(base, &tk, &kv_full[s], 0, c * C, unit);
+                tma_load_3d(base + KB_K, &tk, &kv_full[s], 64, c * C, unit);
+                tma_load_3d(base + SLOT_V, &tv, &kv_full[s], 0, c * C, unit);
+                tma_load_3d(base + SLOT_V + KB_T, &tv, &kv_full[s], 64, c * C, unit);
+                ++kv_issued[s];
+                const int qs = c % QS;
+                if (c >= QS && !bwait(&q_empty[qs], c / QS - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(&q_full[qs], 2 * KB_T);
+                tma_load_3d(sm + SM::Q + qs * 2 * KB_T, &tq, &q_full[qs], 0, c * C, unit);
+                tma_load_3d(sm + SM::Q + qs * 2 * KB_T + KB_T, &tq, &q_full[qs], 64, c * C, unit);
+                ++q_issued[qs];
+            }
+            // Drain: every copy issued has landed before shared memory is released.
+            for (int s = 0; s < NR; ++s)
+                if (kv_issued[s]) bwait(&kv_full[s], kv_issued[s] - 1, abort_f);
+            for (int s = 0; s < QS; ++s)
+                if (q_issued[s]) bwait(&q_full[s], q_issued[s] - 1, abort_f);
+        }
+        __syncwarp();
+    } else if (warp == W_MMA) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_sc_prev = instr_desc(64, 64, FMT_BF16, 0, 0);
+            const uint32_t id_sc_cur = instr_desc(64, 64 + META_ROWS, FMT_BF16, 0, 0);
+            const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
+            const uint32_t id_y1 = instr_desc(128, 64, FMT_BF16, 0, 0);
+            const uint32_t id_y2 = instr_desc(128, 64, FMT_BF16, 1, 0);
+            const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % NR, qs = c % QS;
+                const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
+                if (!bwait(&kv_full[s], c / NR, abort_f) || !bwait(&q_full[qs], c / QS, abort_f) ||
+                    (c >= 1 && !bwait(sc_free, c - 1, abort_f))) { give_up(); break; }
+                tc_fence_after();
+                // window + meta logits
+#pragma unroll
+                for (int j = 0; j <= NP; ++j) {
+                    const int cj = c - NP + j;
+                    if (cj < 0) continue;
+                    const uint32_t kb = sb + SM::KV + (cj % NR) * SLOT;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ss(tmem + T_SC + 64 * j, smem_desc(qb + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
+                                    smem_desc(kb + (kk / 4) * KB_K + (kk % 4) * 32, 16, 1024),
+                                    j == NP ? id_sc_cur : id_sc_prev, kk > 0);
+                }
+                mma_commit(sc_full);
+                mma_commit(&q_empty[qs]);
+                // intra-chunk decayed scores
+                if (!bwait(prep_ready, c, abort_f)) { give_up(); break; }
+                tc_fence_after();
+                if (!unsafe_f[c & 1]) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ss(tmem + TM::A, smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
+                                    smem_desc(sb + SM::KR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_a, kk > 0);
+                }
+                mma_commit(a_full);
+                mma_commit(kr_free);
+                // y^T = S16 QR^T (inter-chunk readout)
+                if (!bwait(s_ready, c, abort_f) || (c >= 1 && !bwait(y_free, c - 1, abort_f))) { give_up(); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8,
+                                   smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
+                mma_commit(qr_free);
+                // y^T += V_band^T W^T
+                if (!bwait(w_full, c, abort_f)) { give_up(); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j <= NP; ++j) {
+                    const int cj = c - NP + j;
+                    if (cj < 0) continue;
+                    const uint32_t vb = sb + SM::KV + (cj % NR) * SLOT + SLOT_V;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + T_Y, smem_desc(vb + kk * 2048, KB_T, 1024),
+                                    smem_desc(sb + SM::W + j * KB_T + kk * 32, 16, 1024), id_y2, 1u);
+                }
+                mma_commit(y_full);
+                mma_commit(w_free);
+                if (NP >= 1 && c - NP >= 0) mma_commit(&kv_empty[(c - NP) % NR]);
+                // S^T += V^T KL
+                {
+                    const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
+                                    smem_desc(sb + SM::KL + kk * 2048, KB_T, 1024), id_st, 1u);
+                }
+                mma_commit(st_done);
+                mma_commit(kl_free);
+                if (NP == 0) mma_commit(&kv_empty[s]);
+            }
+            // Drain: every product issued has completed before tensor memory is released.
+            mma_commit(drain);
+            bwait(drain, 0, abort_f);
+        }
+        __syncwarp();
+    } else if (warp >= W_EPI && warp < W_EPI + 4) {
+        // ------------------------------------------------------ state pass + epilogue
+        const int quarter = warp & 3;
+        const int j = 32 * quarter + lane;  // value dim = tensor-memory lane
+        const uint32_t tl = tmem + tlane(quarter);
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 16) tmem_st16(tl + T_S + cc, z);
+            tmem_wait_st();
+        }
+        const int et = tid - W_EPI * 32;
+        for (int c = 0; c < nchunks; ++c) {
+            const int c0 = c * C, n = min(C, L - c0);
+            bool ok = (c == 0 || bwait(st_done, c - 1, abort_f)) && bwait(prep_ready, c, abort_f);
+            if (!named_bar_and(NB_EPI_R, EPI_N, ok)) { give_up(); break; }
+            tc_fence_after();
+            const float *dv = dec_v + (c & 1) * 128, *ev = er_v + (c & 1) * 128;
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tl + T_S + cb, r0);
+                tmem_ld16(tl + T_S + cb + 16, r1);
+                tmem_wait_ld();
+                uint32_t p16[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    p16[e] = f2_to_bf2(__uint_as_float(r0[2 * e]) * ev[cb + 2 * e],
+                                       __uint_as_float(r0[2 * e + 1]) * ev[cb + 2 * e + 1]);
+                    p16[8 + e] = f2_to_bf2(__uint_as_float(r1[2 * e]) * ev[cb + 16 + 2 * e],
+                                           __uint_as_float(r1[2 * e + 1]) * ev[cb + 16 + 2 * e + 1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    r0[e] = __float_as_uint(__uint_as_float(r0[e]) * dv[cb + e]);
+                    r1[e] = __float_as_uint(__uint_as_float(r1[e]) * dv[cb + 16 + e]);
+                }
+                tmem_st16(tl + T_S16 + cb / 2, p16);
+                tmem_st16(tl + T_S + cb, r0);
+                tmem_st16(tl + T_S + cb + 16, r1);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar(NB_EPI, EPI_N);
+            if (et == 0) mbar_arrive(s_ready);
+            // epilogue: y rows of this chunk
+            ok = bwait(y_full, c, abort_f);
+            if (!named_bar_and(NB_EPI_R, EPI_N, ok)) { give_up(); break; }
+            tc_fence_after();
+            __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
+#pragma unroll 1
+            for (int cc = 0; cc < C; cc += 16) {
+                uint32_t r[16];
+                tmem_ld16(tl + T_Y + cc, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (cc + e < n) yp[(size_t)(cc + e) * D] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            }
+            tc_fence_before();
+            named_bar(NB_EPI, EPI_N);
+            if (et == 0) mbar_arrive(y_free);
+        }
+        // Final state S (row i = key dim): S^T[j][i] -> S_out[i][j].
+        if (!failed && a.S_out) {
+            const bool ok = nchunks == 0 || bwait(st_done, nchunks - 1, abort_f);
+            if (named_bar_and(NB_EPI_R, EPI_N, ok)) {
+                tc_fence_after();
+                float *So = a.S_out + (size_t)unit * D * D + j;
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tl + T_S + cc, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) So[(size_t)(cc + e) * D] = __uint_as_float(r[e]);
+                }
+            } else {
+                give_up();
+            }
+        }
+    } else if (warp >= W_PREP && warp < W_PREP + 8) {
+        // ------------------------------------------------------ gate prep
+        const int tp = tid - W_PREP * 32;
+        const int p = tp & 63, hq = tp >> 6;       // key dims 2p, 2p+1; tokens 16 hq .. 16 hq + 15
+        const uint32_t kblk = (p / 32), kbyte = (p % 32) * 4;
+        const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * D) + p;
+        uint32_t gnext[16];
+        auto load_g = [&](int c) {
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt) {
+                const int tg = c * C + 16 * hq + tt;
+                gnext[tt] = tg < L ? gp[(size_t)tg * (D / 2)] : 0x7F807F80u;  // +inf: no decay
+            }
+        };
+        if (nchunks > 0) load_g(0);
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % NR, qs = c % QS;
+            // 1. log-gates and the quarter's prefix sums (base 2)
+            float2 cs[16];
+            {
+                float ra = 0.f, rb = 0.f;
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const float2 gg = bf2_to_f2(gnext[tt]);
+                    ra += log2_sigmoid(gg.x);
+                    rb += log2_sigmoid(gg.y);
+                    cs[tt] = make_float2(ra, rb);
+                }
+                tot[hq * 128 + 2 * p] = ra;
+                tot[hq * 128 + 2 * p + 1] = rb;
+            }
+            if (c + 1 < nchunks) load_g(c + 1);
+            named_bar(NB_PREP, PREP_N);
+            // 2. chunk offsets: r = b at token 31, b_last = b at token 63
+            float2 T[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) T[qq] = make_float2(tot[qq * 128 + 2 * p], tot[qq * 128 + 2 * p + 1]);
+            const float2 half0 = make_float2(T[0].x + T[1].x, T[0].y + T[1].y);
+            const float2 half1 = make_float2(T[2].x + T[3].x, T[2].y + T[3].y);
+            float2 pre = make_float2(0.f, 0.f);  // b at the end of the previous quarter
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+                if (qq < hq) { pre.x += T[qq].x; pre.y += T[qq].y; }
+            if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[c & 1] = 1;
+            const bool ok_in = bwait(&kv_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
+            if (!named_bar_and(NB_PREP_R, PREP_N, ok_in)) { give_up(); break; }
+            const bool unsafe = unsafe_f[c & 1] != 0;
+            const uint8_t *kraw = sm + SM::KV + s * SLOT + kblk * KB_K;
+            const uint8_t *qraw = sm + SM::Q + qs * 2 * KB_T + kblk * KB_T;
+            const float2 blast = make_float2(half0.x + half1.x, half0.y + half1.y);
+            if (!unsafe) {
+                // b_t - r for this thread's tokens: cs + (pre - half0)
+                const float2 o = make_float2(pre.x - half0.x, pre.y - half0.y);
+                const float2 F = make_float2(ex2(blast.x - half0.x), ex2(blast.y - half0.y));  // 2^{b_last - r}
+                uint32_t klp[16];
+                bool ok = c == 0 || bwait(kr_free, c - 1, abort_f);
+                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const int t = 16 * hq + tt;
+                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + sw128_offset(t, kbyte)));
+                    const float ka = kv.x * exp2_fma(-(cs[tt].x + o.x)), kb2 = kv.y * exp2_fma(-(cs[tt].y + o.y));
+                    *reinterpret_cast<uint32_t *>(sm + SM::KR + kblk * KB_T + sw128_offset(t, kbyte)) = f2_to_bf2(ka, kb2);
+                    klp[tt] = f2_to_bf2(ka * F.x, kb2 * F.y);
+                }
+                ok = c == 0 || bwait(qr_free, c - 1, abort_f);
+                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const int t = 16 * hq + tt;
+                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + sw128_offset(t, kbyte)));
+                    *reinterpret_cast<uint32_t *>(sm + SM::QR + kblk * KB_T + sw128_offset(t, kbyte)) =
+                        f2_to_bf2(qv.x * ex2(cs[tt].x + o.x), qv.y * ex2(cs[tt].y + o.y));
+                }
+                ok = c == 0 || bwait(kl_free, c - 1, abort_f);
+                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt)
+                    *reinterpret_cast<uint32_t *>(sm + SM::KL + kblk * KB_T + sw128_offset(16 * hq + tt, kbyte)) = klp[tt];
+                if (hq == 0) {
+                    er_v[(c & 1) * 128 + 2 * p] = ex2(half0.x);
+                    er_v[(c & 1) * 128 + 2 * p + 1] = ex2(half0.y);
+                }
+            } else {
+                // Exact intra-chunk scores on the CUDA cores.  Scratch: the
+                // KL and W tiles hold b (fp32, [64][128]) meanwhile.
+                bool ok = (c == 0 || (bwait(kl_free, c - 1, abort_f) && bwait(w_free, c - 1, abort_f) &&
+                                      bwait(sc_free, c - 1, abort_f) && bwait(kr_free, c - 1, abort_f) &&
+                                      bwait(qr_free, c - 1, abort_f)));
+                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+                float *bz = reinterpret_cast<float *>(sm + SM::KL);
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt)
+                    *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) =
+                        make_float2(cs[tt].x + pre.x, cs[tt].y + pre.y);
+                named_bar(NB_PREP, PREP_N);
+                {
+                    const int quarter = warp & 3, li = ((warp - W_PREP) >> 2) * 32 + lane;
+                    const int t = 16 * quarter + (li & 15), s0 = 16 * (li >> 4);
+                    const uint8_t *qrow = sm + SM::Q + qs * 2 * KB_T;
+                    const uint8_t *krow = sm + SM::KV + s * SLOT;
+                    float acc[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                    for (int i = 0; i < D; ++i) {
+                        const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                            qrow + (i / 64) * KB_T + sw128_offset(t, (i % 64) * 2)));
+                        const float bt = bz[t * D + i];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int sk = s0 + e;
+                            if (sk <= t) {
+                                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                    krow + (i / 64) * KB_K + sw128_offset(sk, (i % 64) * 2)));
+                                acc[e] += qv * kv * ex2(bt - bz[sk * D + i]);
+                            }
+                        }
+                    }
+                    uint32_t r[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(acc[e]);
+                    tmem_st16_x2<16>(tmem + tlane(quarter) + TM::A + 32 * ((warp - W_PREP) >> 2), r);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                named_bar(NB_PREP, PREP_N);
+                if (tp == 0) mbar_arrive(a_full);
+                // QR with r = 0 (exponents <= 0), KL exact.
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const int t = 16 * hq + tt;
+                    const float2 bt = make_float2(cs[tt].x + pre.x, cs[tt].y + pre.y);
+                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + sw128_offset(t, kbyte)));
+                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + sw128_offset(t, kbyte)));
+                    *reinterpret_cast<uint32_t *>(sm + SM::QR + kblk * KB_T + sw128_offset(t, kbyte)) =
+                        f2_to_bf2(qv.x * ex2(bt.x), qv.y * ex2(bt.y));
+                    *reinterpret_cast<uint32_t *>(sm + SM::KL + kblk * KB_T + sw128_offset(t, kbyte)) =
+                        f2_to_bf2(kv.x * ex2(blast.x - bt.x), kv.y * ex2(blast.y - bt.y));
+                }
+                if (hq == 0) {
+                    er_v[(c & 1) * 128 + 2 * p] = 1.f;
+                    er_v[(c & 1) * 128 + 2 * p + 1] = 1.f;
+                }
+            }
+            if (hq == 0) {
+                dec_v[(c & 1) * 128 + 2 * p] = ex2(blast.x);
+                dec_v[(c & 1) * 128 + 2 * p + 1] = ex2(blast.y);
+            }
+            fence_proxy_async_smem();
+            named_bar(NB_PREP, PREP_N);
+            if (tp == 0) {
+                unsafe_f[(c + 1) & 1] = 0;  // the MMA issuer read it for chunk c - 1 before state_{c-1}
+                mbar_arrive(prep_ready);
+                if (!unsafe) mbar_arrive(a_full);
+                mbar_arrive(&q_empty[qs]);
+            }
+        }
+        // State hand-off: the last min(L, w) keys and values into the ring, pos = L.
+        if (!failed && a.S_out) {
+            const int first = max(0, L - w);
+            const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
+            __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
+            for (int e = tp; e < (L - first) * (D / 8); e += PREP_N) {
+                const int tau = first + e / (D / 8), i8 = (e % (D / 8)) * 8;
+                *reinterpret_cast<uint4 *>(rk + (size_t)(tau % w) * D + i8) =
+                    *reinterpret_cast<const uint4 *>(kp + (size_t)tau * D + i8);
+                *reinterpret_cast<uint4 *>(rv + (size_t)(tau % w) * D + i8) =
+                    *reinterpret_cast<const uint4 *>(vp + (size_t)tau * D + i8);
+            }
+            if (h == 0 && tp == 0) a.pos[unit / a.H] = L;
+        }
+    } else {
+        // ------------------------------------------------------ window softmax
+        const int quarter = warp & 3, hs = lane >> 4;
+        const int t = 16 * quarter + (lane & 15);
+        const uint32_t tl = tmem + tlane(quarter);
+        const int st_ = tid - W_SOFT * 32;
+        for (int c = 0; c < nchunks; ++c) {
+            const int c0 = c * C, n = min(C, L - c0), tg = c0 + t;
+            const bool rowok = t < n;
+            const int pbase = c0 - 64 * NP;  // global position of band column 0
+            bool ok = bwait(sc_full, c, abort_f) && bwait(a_full, c, abort_f);
+            if (!named_bar_and(NB_SOFT_R, SOFT_N, ok)) { give_up(); break; }
+            tc_fence_after();
+            // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
+            float x[2 * NB][16];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < 2 * NB; ++jj) {
+                uint32_t r[16];
+                tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int pp = pbase + 32 * jj + 16 * hs + e;
+                    const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
+                    x[jj][e] = valid ? __uint_as_float(r[e]) : -INFINITY;
+                    mx = fmaxf(mx, x[jj][e]);
+                }
+            }
+            float meta[META_ROWS];
+            {
+                uint32_t r[16];
+                tmem_ld16(tl + T_SC + 64 * NB, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < META_ROWS; ++e) {
+                    meta[e] = (hs == 0 && e < m) ? __uint_as_float(r[e]) : -INFINITY;
+                    mx = fmaxf(mx, meta[e]);
+                }
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float M2 = mx * LOG2E;
+            float sum = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 2 * NB; ++jj)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    x[jj][e] = ex2(fmaf(x[jj][e], LOG2E, -M2));
+                    sum += x[jj][e];
+                }
+#pragma unroll
+            for (int e = 0; e < META_ROWS; ++e)
+                if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+            const float inv = a.alpha / sum;
+            ok = c == 0 || bwait(w_free, c - 1, abort_f);
+            if (!named_bar_and(NB_SOFT_R, SOFT_N, ok)) { give_up(); break; }
+#pragma unroll
+            for (int jj = 0; jj < 2 * NB; ++jj) {
+                const int col0 = 32 * jj + 16 * hs;  // this thread's band columns col0 .. col0 + 15
+                uint32_t ra[16];
+                const bool cur = jj >= 2 * NP;       // current chunk: add the intra-chunk scores
+                if (cur) {
+                    tmem_ld16_x2<16>(tl + TM::A + 32 * (jj - 2 * NP), ra);
+                    tmem_wait_ld();
+                }
+                uint32_t packed[8];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    float wv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = col0 + e + u, sidx = col - 64 * NP;
+                        float v = x[jj][e + u] * inv;
+                        if (cur && sidx <= t) v += __uint_as_float(ra[e + u]);
+                        wv[u] = rowok ? v : 0.f;
+                    }
+                    packed[e / 2] = f2_to_bf2(wv[0], wv[1]);
+                }
+                const uint32_t blk = (col0 / 64) * KB_T, byte = (col0 % 64) * 2;
+                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
+                    make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(NB_SOFT, SOFT_N);
+            if (st_ == 0) {
+                mbar_arrive(sc_free);
+                mbar_arrive(w_full);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == W_MMA) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace ws
+}  // namespace lizard
