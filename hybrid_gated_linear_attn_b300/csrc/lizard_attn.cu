@@ -133,13 +133,13 @@ static int sm_count()
 
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                          const ws::WsArgs &wa, int units, cudaStream_t s)
+                                          const CUtensorMap &tg, const ws::WsArgs &wa, int units, cudaStream_t s)
 {
     auto kern = ws::prefill_ws_kernel<NP>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<units, ws::THREADS, smem, s>>>(tq, tk, tv, wa);
+    kern<<<units, ws::THREADS, smem, s>>>(tq, tk, tv, tg, wa);
     return launch_status();
 }
 
@@ -147,16 +147,16 @@ static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorM
 static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s)
 {
     const int units = pa.B * pa.H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tg;
     if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
-        !make_token_map(&tv, pa.v, units, pa.L))
+        !make_token_map(&tv, pa.v, units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
         return LIZARD_ERR_CUDA;
     ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m};
-    return pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, wa, units, s)
-                     : launch_prefill_ws_np<1>(tq, tk, tv, wa, units, s);
+    return pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units, s)
+                     : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units, s);
 }
 
 template <typename T, int D>

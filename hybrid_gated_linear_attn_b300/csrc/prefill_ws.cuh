@@ -27,12 +27,15 @@
 // (sum_i q k 2^{b_t - b_s}, exponent <= 0), and its QR uses r = 0.  So every
 // gate value is handled.
 //
-// Warp roles (18 warps):
-//   warp 0       TMA producer: q tiles (2 stages), k/v tiles (ring of NP+2)
-//   warp 1       MMA issuer (one thread): all tcgen05.mma, commits
-//   warps 2-5    state pass (S^T decay, S16) and y epilogue; the final state
-//   warps 6-13   gate prep: log-sigmoid, prefix sums, QR / KR / KL operands
-//   warps 14-17  window softmax: W from SC and A
+// Warp roles (19 warps):
+//   warp 0       TMA producer: g and q tiles, k/v tiles (ring of NP+2)
+//   warp 1       MMA issuer (one thread): scores, A and the state update
+//   warp 2       MMA issuer (one thread): the two output products
+//   warps 3-6    state pass (S^T decay, S16) and y epilogue; the final state
+//   warps 7-14   gate prep: log-sigmoid, prefix sums, QR / KR / KL operands
+//   warps 15-18  window softmax: W from SC and A
+// Two issuers keep the state chain (scores, A, state update) from queueing
+// behind the output products, which wait for the softmax.
 // Every hand-off is an mbarrier; every wait is bounded (a timeout records
 // DEV_TIMEOUT, drains the copies and products in flight, and returns).
 #pragma once
@@ -47,9 +50,9 @@ using namespace sm100;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NWARPS = 18;
+constexpr int NWARPS = 19;
 constexpr int THREADS = NWARPS * 32;
-constexpr int W_TMA = 0, W_MMA = 1, W_EPI = 2, W_PREP = 6, W_SOFT = 14;
+constexpr int W_TMA = 0, W_MMA = 1, W_MMAY = 2, W_EPI = 3, W_PREP = 7, W_SOFT = 15;
 constexpr int EPI_N = 128, PREP_N = 256, SOFT_N = 128;
 enum : int { NB_EPI = 1, NB_PREP = 2, NB_SOFT = 3, NB_EPI_R = 4, NB_PREP_R = 5, NB_SOFT_R = 6 };
 constexpr int META_ROWS = 16;
@@ -69,7 +72,8 @@ struct Smem {
     static constexpr int NR = NP + 2;
     static constexpr uint32_t KV = 0;
     static constexpr uint32_t Q = KV + NR * SLOT;
-    static constexpr uint32_t QR = Q + QS * 2 * KB_T;
+    static constexpr uint32_t G = Q + QS * 2 * KB_T;       // gate logits of one chunk
+    static constexpr uint32_t QR = G + 2 * KB_T;
     static constexpr uint32_t KR = QR + 2 * KB_T;
     static constexpr uint32_t KL = KR + 2 * KB_T;
     static constexpr uint32_t W = KL + 2 * KB_T;           // KL and W: 32 KB of exact-A scratch
@@ -77,10 +81,11 @@ struct Smem {
     static constexpr uint32_t VEC = W + W_BYTES;           // dec[2][128], er[2][128], tot[4][128] (fp32)
     static constexpr uint32_t FLAG = VEC + (2 * 128 + 2 * 128 + 4 * 128) * 4;  // unsafe[2], abort
     static constexpr uint32_t BAR = FLAG + 16;
-    static constexpr int NBAR = 2 * QS + 2 * NR + 14;
+    static constexpr int NBAR = 2 * QS + 4 * NR + 17;
     static constexpr uint32_t TSLOT = BAR + NBAR * 8;
     static constexpr uint32_t USED = TSLOT + 16;
     static constexpr uint32_t BYTES = USED + 1024;
+    static_assert(BYTES <= 232448, "shared memory budget");
 };
 
 // Tensor-memory columns (512 allocated).
@@ -140,6 +145,51 @@ __device__ __forceinline__ float log2_sigmoid(float g)
     p = fmaf(p, u, 1.4426640f);
     return fminf(g, 0.f) * LOG2E - u * p;
 }
+// Packed fp32x2 arithmetic (one instruction for a pair of key dims).
+__device__ __forceinline__ uint64_t pk2(float2 a)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t r)
+{
+    float2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+    return upk2(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+    return upk2(r);
+}
+// log2_sigmoid of a pair, the polynomial in packed arithmetic.
+__device__ __forceinline__ float2 log2_sigmoid2(float2 g)
+{
+    const float2 u = make_float2(ex2(-fabsf(g.x) * LOG2E), ex2(-fabsf(g.y) * LOG2E));
+    float2 p = make_float2(0.015127916f, 0.015127916f);
+    p = fma2(p, u, make_float2(-0.078158207f, -0.078158207f));
+    p = fma2(p, u, make_float2(0.19238505f, 0.19238505f));
+    p = fma2(p, u, make_float2(-0.32461637f, -0.32461637f));
+    p = fma2(p, u, make_float2(0.47311336f, 0.47311336f));
+    p = fma2(p, u, make_float2(-0.72051549f, -0.72051549f));
+    p = fma2(p, u, make_float2(1.4426640f, 1.4426640f));
+    const float2 mn = make_float2(fminf(g.x, 0.f) * LOG2E, fminf(g.y, 0.f) * LOG2E);
+    return fma2(make_float2(-u.x, -u.y), p, mn);
+}
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
 {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
@@ -178,7 +228,7 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int 
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const WsArgs a)
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const WsArgs a)
 {
     using SM = Smem<NP>;
     using TM = Tmem<NP>;
@@ -193,12 +243,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *unsafe_f = reinterpret_cast<volatile int *>(sm + SM::FLAG);  // [2]
     volatile int *abort_f = unsafe_f + 2;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::BAR);
-    uint64_t *q_full = bars, *q_empty = bars + QS, *kv_full = bars + 2 * QS, *kv_empty = kv_full + NR;
-    uint64_t *prep_ready = kv_empty + NR, *kr_free = prep_ready + 1, *qr_free = prep_ready + 2,
+    // k and v of a slot load and free separately: a key tile is free once
+    // the band scores that read it are done, a value tile only after the
+    // output products.
+    uint64_t *q_full = bars, *q_empty = bars + QS, *k_full = bars + 2 * QS, *k_empty = k_full + NR;
+    uint64_t *v_full = k_empty + NR, *v_empty = v_full + NR;
+    uint64_t *g_full = v_empty + NR, *g_empty = g_full + 1;
+    uint64_t *prep_ready = g_empty + 1, *kr_free = prep_ready + 1, *qr_free = prep_ready + 2,
              *kl_free = prep_ready + 3, *sc_full = prep_ready + 4, *a_full = prep_ready + 5,
              *sc_free = prep_ready + 6, *w_full = prep_ready + 7, *w_free = prep_ready + 8,
              *s_ready = prep_ready + 9, *st_done = prep_ready + 10, *y_full = prep_ready + 11,
-             *y_free = prep_ready + 12, *drain = prep_ready + 13;
+             *y_free = prep_ready + 12, *drain = prep_ready + 13, *drain_y = prep_ready + 14;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM::TSLOT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -217,10 +272,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&q_empty[i], 2);
         }
         for (int i = 0; i < NR; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 14; ++i) mbar_init(&prep_ready[i], i == 5 ? 2 : 1);  // a_full: MMA + prep
+        mbar_init(g_full, 1);
+        mbar_init(g_empty, 1);
+        for (int i = 0; i < 15; ++i) mbar_init(&prep_ready[i], i == 5 ? 2 : 1);  // a_full: MMA + prep
         unsafe_f[0] = 0;
         unsafe_f[1] = 0;
         *abort_f = 0;
@@ -228,6 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        prefetch_tmap(&tg);
     }
     // Meta keys of this head into rows 64..79 of every key tile (zero past m).
     for (int e = tid; e < NR * META_ROWS * 64; e += THREADS) {
@@ -254,44 +314,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == W_TMA) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t kv_issued[NR] = {}, q_issued[QS] = {};
+            uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {}, g_issued = 0;
             for (int c = 0; c < nchunks && !failed; ++c) {
+                if (c >= 1 && !bwait(g_empty, c - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(g_full, 2 * KB_T);
+                tma_load_3d(sm + SM::G, &tg, g_full, 0, c * C, unit);
+                tma_load_3d(sm + SM::G + KB_T, &tg, g_full, 64, c * C, unit);
+                ++g_issued;
                 const int s = c % NR;
-                if (c >= NR && !bwait(&kv_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
                 uint8_t *base = sm + SM::KV + s * SLOT;
-                mbar_arrive_expect_tx(&kv_full[s], 2 * KB_T + 2 * KB_T);
-                tma_load_3d(base, &tk, &kv_full[s], 0, c * C, unit);
-                tma_load_3d(base + KB_K, &tk, &kv_full[s], 64, c * C, unit);
-                tma_load_3d(base + SLOT_V, &tv, &kv_full[s], 0, c * C, unit);
-                tma_load_3d(base + SLOT_V + KB_T, &tv, &kv_full[s], 64, c * C, unit);
-                ++kv_issued[s];
+                if (c >= NR && !bwait(&k_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
+                tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
+                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                ++k_issued[s];
                 const int qs = c % QS;
                 if (c >= QS && !bwait(&q_empty[qs], c / QS - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&q_full[qs], 2 * KB_T);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T, &tq, &q_full[qs], 0, c * C, unit);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T + KB_T, &tq, &q_full[qs], 64, c * C, unit);
                 ++q_issued[qs];
+                if (c >= NR && !bwait(&v_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
+                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
+                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                ++v_issued[s];
             }
             // Drain: every copy issued has landed before shared memory is released.
-            for (int s = 0; s < NR; ++s)
-                if (kv_issued[s]) bwait(&kv_full[s], kv_issued[s] - 1, abort_f);
+            for (int s = 0; s < NR; ++s) {
+                if (k_issued[s]) bwait(&k_full[s], k_issued[s] - 1, abort_f);
+                if (v_issued[s]) bwait(&v_full[s], v_issued[s] - 1, abort_f);
+            }
             for (int s = 0; s < QS; ++s)
                 if (q_issued[s]) bwait(&q_full[s], q_issued[s] - 1, abort_f);
+            if (g_issued) bwait(g_full, g_issued - 1, abort_f);
         }
         __syncwarp();
     } else if (warp == W_MMA) {
-        // ------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------ MMA issuer: scores, A, state
         if (lane == 0) {
             const uint32_t id_sc_prev = instr_desc(64, 64, FMT_BF16, 0, 0);
             const uint32_t id_sc_cur = instr_desc(64, 64 + META_ROWS, FMT_BF16, 0, 0);
             const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
-            const uint32_t id_y1 = instr_desc(128, 64, FMT_BF16, 0, 0);
-            const uint32_t id_y2 = instr_desc(128, 64, FMT_BF16, 1, 0);
             const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % NR, qs = c % QS;
                 const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
-                if (!bwait(&kv_full[s], c / NR, abort_f) || !bwait(&q_full[qs], c / QS, abort_f) ||
+                if (!bwait(&k_full[s], c / NR, abort_f) || !bwait(&q_full[qs], c / QS, abort_f) ||
                     (c >= 1 && !bwait(sc_free, c - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
                 // window + meta logits
@@ -319,16 +388,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mma_commit(a_full);
                 mma_commit(kr_free);
+                // The key tile of chunk c - NP has no reader left: the last
+                // band scores that use it were issued above, and its raw keys
+                // were read by the prep of chunk c - NP (done: prep_ready).
+                if (c - NP >= 0) mma_commit(&k_empty[(c - NP) % NR]);
+                // S^T += V^T KL (S^T decayed by the state pass)
+                if (!bwait(s_ready, c, abort_f) || !bwait(&v_full[s], c / NR, abort_f)) { give_up(); break; }
+                tc_fence_after();
+                {
+                    const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
+                                    smem_desc(sb + SM::KL + kk * 2048, KB_T, 1024), id_st, 1u);
+                }
+                mma_commit(st_done);
+                mma_commit(kl_free);
+            }
+            // Drain: every product issued has completed before tensor memory is released.
+            mma_commit(drain);
+            bwait(drain, 0, abort_f);
+        }
+        __syncwarp();
+    } else if (warp == W_MMAY) {
+        // ------------------------------------------------------ MMA issuer: outputs
+        if (lane == 0) {
+            const uint32_t id_y1 = instr_desc(128, 64, FMT_BF16, 0, 0);
+            const uint32_t id_y2 = instr_desc(128, 64, FMT_BF16, 1, 0);
+            for (int c = 0; c < nchunks; ++c) {
                 // y^T = S16 QR^T (inter-chunk readout)
-                if (!bwait(s_ready, c, abort_f) || (c >= 1 && !bwait(y_free, c - 1, abort_f))) { give_up(); break; }
+                if (!bwait(prep_ready, c, abort_f) || !bwait(s_ready, c, abort_f) ||
+                    (c >= 1 && !bwait(y_free, c - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8,
-                                   smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
+                                smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
                 mma_commit(qr_free);
                 // y^T += V_band^T W^T
-                if (!bwait(w_full, c, abort_f)) { give_up(); break; }
+                if (!bwait(w_full, c, abort_f) || !bwait(&v_full[c % NR], c / NR, abort_f) ||
+                    (NP == 0 && !bwait(st_done, c, abort_f))) { give_up(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j <= NP; ++j) {
@@ -342,22 +441,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mma_commit(y_full);
                 mma_commit(w_free);
-                if (NP >= 1 && c - NP >= 0) mma_commit(&kv_empty[(c - NP) % NR]);
-                // S^T += V^T KL
-                {
-                    const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
-                                    smem_desc(sb + SM::KL + kk * 2048, KB_T, 1024), id_st, 1u);
-                }
-                mma_commit(st_done);
-                mma_commit(kl_free);
-                if (NP == 0) mma_commit(&kv_empty[s]);
+                // The value tile of chunk c - NP has no reader left: its state
+                // update (issued before A_c, which the softmax waited for;
+                // for NP = 0 st_done above) and these products.
+                if (c - NP >= 0) mma_commit(&v_empty[(c - NP) % NR]);
             }
-            // Drain: every product issued has completed before tensor memory is released.
-            mma_commit(drain);
-            bwait(drain, 0, abort_f);
+            mma_commit(drain_y);
+            bwait(drain_y, 0, abort_f);
         }
         __syncwarp();
     } else if (warp >= W_EPI && warp < W_EPI + 4) {
@@ -376,7 +466,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int et = tid - W_EPI * 32;
         for (int c = 0; c < nchunks; ++c) {
             const int c0 = c * C, n = min(C, L - c0);
-            bool ok = (c == 0 || bwait(st_done, c - 1, abort_f)) && bwait(prep_ready, c, abort_f);
+            bool ok = (c == 0 || (bwait(st_done, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f))) &&
+                      bwait(prep_ready, c, abort_f);
             if (!named_bar_and(NB_EPI_R, EPI_N, ok)) { give_up(); break; }
             tc_fence_after();
             const float *dv = dec_v + (c & 1) * 128, *ev = er_v + (c & 1) * 128;
@@ -448,34 +539,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int tp = tid - W_PREP * 32;
         const int p = tp & 63, hq = tp >> 6;       // key dims 2p, 2p+1; tokens 16 hq .. 16 hq + 15
         const uint32_t kblk = (p / 32), kbyte = (p % 32) * 4;
-        const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * D) + p;
-        uint32_t gnext[16];
-        auto load_g = [&](int c) {
-#pragma unroll
-            for (int tt = 0; tt < 16; ++tt) {
-                const int tg = c * C + 16 * hq + tt;
-                gnext[tt] = tg < L ? gp[(size_t)tg * (D / 2)] : 0x7F807F80u;  // +inf: no decay
-            }
-        };
-        if (nchunks > 0) load_g(0);
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % NR, qs = c % QS;
-            // 1. log-gates and the quarter's prefix sums (base 2)
+            const int n = min(C, L - c * C);
+            if (!named_bar_and(NB_PREP_R, PREP_N, bwait(g_full, c, abort_f))) { give_up(); break; }
+            // 1. log-gates and the quarter's prefix sums (base 2); tokens past
+            //    the end of the sequence get no decay.
             float2 cs[16];
             {
-                float ra = 0.f, rb = 0.f;
+                float2 run = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) {
-                    const float2 gg = bf2_to_f2(gnext[tt]);
-                    ra += log2_sigmoid(gg.x);
-                    rb += log2_sigmoid(gg.y);
-                    cs[tt] = make_float2(ra, rb);
+                    const int t = 16 * hq + tt;
+                    const float2 gg = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + SM::G + kblk * KB_T +
+                                                                                   sw128_offset(t, kbyte)));
+                    const float2 l = log2_sigmoid2(gg);
+                    if (t < n) run = add2(run, l);
+                    cs[tt] = run;
                 }
-                tot[hq * 128 + 2 * p] = ra;
-                tot[hq * 128 + 2 * p + 1] = rb;
+                tot[hq * 128 + 2 * p] = run.x;
+                tot[hq * 128 + 2 * p + 1] = run.y;
             }
-            if (c + 1 < nchunks) load_g(c + 1);
             named_bar(NB_PREP, PREP_N);
+            if (tp == 0) mbar_arrive(g_empty);  // every prep thread has read this chunk's g
             // 2. chunk offsets: r = b at token 31, b_last = b at token 63
             float2 T[4];
 #pragma unroll
@@ -487,7 +573,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int qq = 0; qq < 4; ++qq)
                 if (qq < hq) { pre.x += T[qq].x; pre.y += T[qq].y; }
             if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[c & 1] = 1;
-            const bool ok_in = bwait(&kv_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
+            const bool ok_in = bwait(&k_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
             if (!named_bar_and(NB_PREP_R, PREP_N, ok_in)) { give_up(); break; }
             const bool unsafe = unsafe_f[c & 1] != 0;
             const uint8_t *kraw = sm + SM::KV + s * SLOT + kblk * KB_K;
@@ -496,32 +582,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!unsafe) {
                 // b_t - r for this thread's tokens: cs + (pre - half0)
                 const float2 o = make_float2(pre.x - half0.x, pre.y - half0.y);
-                const float2 F = make_float2(ex2(blast.x - half0.x), ex2(blast.y - half0.y));  // 2^{b_last - r}
-                uint32_t klp[16];
-                bool ok = c == 0 || bwait(kr_free, c - 1, abort_f);
+                const float2 F = make_float2(ex2(half1.x), ex2(half1.y));  // 2^{b_last - r}
+                const bool ok = c == 0 || (bwait(kr_free, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f) &&
+                                           bwait(kl_free, c - 1, abort_f));
                 if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+                uint8_t *kr_t = sm + SM::KR + kblk * KB_T, *qr_t = sm + SM::QR + kblk * KB_T;
+                uint8_t *kl_t = sm + SM::KL + kblk * KB_T;
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) {
-                    const int t = 16 * hq + tt;
-                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + sw128_offset(t, kbyte)));
-                    const float ka = kv.x * exp2_fma(-(cs[tt].x + o.x)), kb2 = kv.y * exp2_fma(-(cs[tt].y + o.y));
-                    *reinterpret_cast<uint32_t *>(sm + SM::KR + kblk * KB_T + sw128_offset(t, kbyte)) = f2_to_bf2(ka, kb2);
-                    klp[tt] = f2_to_bf2(ka * F.x, kb2 * F.y);
+                    const uint32_t off = sw128_offset(16 * hq + tt, kbyte);
+                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
+                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
+                    const float2 e = add2(cs[tt], o);
+                    const float2 kr = mul2(kv, make_float2(ex2(-e.x), ex2(-e.y)));
+                    const float2 qr = mul2(qv, make_float2(ex2(e.x), ex2(e.y)));
+                    const float2 kl = mul2(kr, F);
+                    *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
+                    *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
+                    *reinterpret_cast<uint32_t *>(kl_t + off) = f2_to_bf2(kl.x, kl.y);
                 }
-                ok = c == 0 || bwait(qr_free, c - 1, abort_f);
-                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
-#pragma unroll
-                for (int tt = 0; tt < 16; ++tt) {
-                    const int t = 16 * hq + tt;
-                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + sw128_offset(t, kbyte)));
-                    *reinterpret_cast<uint32_t *>(sm + SM::QR + kblk * KB_T + sw128_offset(t, kbyte)) =
-                        f2_to_bf2(qv.x * ex2(cs[tt].x + o.x), qv.y * ex2(cs[tt].y + o.y));
-                }
-                ok = c == 0 || bwait(kl_free, c - 1, abort_f);
-                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
-#pragma unroll
-                for (int tt = 0; tt < 16; ++tt)
-                    *reinterpret_cast<uint32_t *>(sm + SM::KL + kblk * KB_T + sw128_offset(16 * hq + tt, kbyte)) = klp[tt];
                 if (hq == 0) {
                     er_v[(c & 1) * 128 + 2 * p] = ex2(half0.x);
                     er_v[(c & 1) * 128 + 2 * p + 1] = ex2(half0.y);
@@ -629,28 +708,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
             float x[2 * NB][16];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int jj = 0; jj < 2 * NB; ++jj) {
-                uint32_t r[16];
-                tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int pp = pbase + 32 * jj + 16 * hs + e;
-                    const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
-                    x[jj][e] = valid ? __uint_as_float(r[e]) : -INFINITY;
-                    mx = fmaxf(mx, x[jj][e]);
-                }
-            }
             float meta[META_ROWS];
+            float mx = -INFINITY;
             {
-                uint32_t r[16];
-                tmem_ld16(tl + T_SC + 64 * NB, r);
+                uint32_t r[2 * NB][16], rm[16];
+#pragma unroll
+                for (int jj = 0; jj < 2 * NB; ++jj) tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r[jj]);
+                tmem_ld16(tl + T_SC + 64 * NB, rm);
                 tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 2 * NB; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int pp = pbase + 32 * jj + 16 * hs + e;
+                        const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
+                        x[jj][e] = valid ? __uint_as_float(r[jj][e]) : -INFINITY;
+                        mx = fmaxf(mx, x[jj][e]);
+                    }
 #pragma unroll
                 for (int e = 0; e < META_ROWS; ++e) {
-                    meta[e] = (hs == 0 && e < m) ? __uint_as_float(r[e]) : -INFINITY;
+                    meta[e] = (hs == 0 && e < m) ? __uint_as_float(rm[e]) : -INFINITY;
                     mx = fmaxf(mx, meta[e]);
                 }
             }
@@ -671,15 +748,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float inv = a.alpha / sum;
             ok = c == 0 || bwait(w_free, c - 1, abort_f);
             if (!named_bar_and(NB_SOFT_R, SOFT_N, ok)) { give_up(); break; }
+            uint32_t ra2[2][16];  // intra-chunk scores of this thread's current-chunk columns
+            tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
+            tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
+            tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 2 * NB; ++jj) {
                 const int col0 = 32 * jj + 16 * hs;  // this thread's band columns col0 .. col0 + 15
-                uint32_t ra[16];
                 const bool cur = jj >= 2 * NP;       // current chunk: add the intra-chunk scores
-                if (cur) {
-                    tmem_ld16_x2<16>(tl + TM::A + 32 * (jj - 2 * NP), ra);
-                    tmem_wait_ld();
-                }
+                const uint32_t *ra = ra2[cur ? jj - 2 * NP : 0];
                 uint32_t packed[8];
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
