@@ -120,17 +120,6 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
     return launch_status();
 }
 
-static int sm_count()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 1;
-    }
-    return n;
-}
-
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                           const CUtensorMap &tg, const ws::WsArgs &wa, int units, cudaStream_t s)

@@ -214,6 +214,23 @@ __device__ __forceinline__ bool named_bar_and(int id, int n, bool p)
         : "memory");
     return r != 0;
 }
+// A role-wide wait: lane 0 of the role's first warp polls the mbarriers
+// (`poll`), the role's other warps block in a named barrier meanwhile, so a
+// waiting role takes no issue slots.  The AND-reduction barrier hands every
+// thread the same verdict.  Readers of data produced by the async proxy or
+// the tensor cores are ordered after the poller's acquire by this barrier
+// (and by tcgen05.fence::after_thread_sync for tensor memory).
+template <typename Poll>
+__device__ __forceinline__ bool role_wait(bool leader_warp, int lane, int id, int n, Poll poll)
+{
+    bool ok = true;
+    if (leader_warp) {
+        if (lane == 0) ok = poll();
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    return named_bar_and(id, n, ok);
+}
 // Bounded wait on phase `use` (its parity) of an mbarrier; false on timeout
 // or when another role already gave up.
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int *abort_flag)
@@ -466,9 +483,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int et = tid - W_EPI * 32;
         for (int c = 0; c < nchunks; ++c) {
             const int c0 = c * C, n = min(C, L - c0);
-            bool ok = (c == 0 || (bwait(st_done, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f))) &&
-                      bwait(prep_ready, c, abort_f);
-            if (!named_bar_and(NB_EPI_R, EPI_N, ok)) { give_up(); break; }
+            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] {
+                    return (c == 0 || (bwait(st_done, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f))) &&
+                           bwait(prep_ready, c, abort_f);
+                })) { give_up(); break; }
             tc_fence_after();
             const float *dv = dec_v + (c & 1) * 128, *ev = er_v + (c & 1) * 128;
 #pragma unroll 1
@@ -499,8 +517,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             named_bar(NB_EPI, EPI_N);
             if (et == 0) mbar_arrive(s_ready);
             // epilogue: y rows of this chunk
-            ok = bwait(y_full, c, abort_f);
-            if (!named_bar_and(NB_EPI_R, EPI_N, ok)) { give_up(); break; }
+            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] { return bwait(y_full, c, abort_f); })) {
+                give_up();
+                break;
+            }
             tc_fence_after();
             __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
 #pragma unroll 1
@@ -518,8 +538,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // Final state S (row i = key dim): S^T[j][i] -> S_out[i][j].
         if (!failed && a.S_out) {
-            const bool ok = nchunks == 0 || bwait(st_done, nchunks - 1, abort_f);
-            if (named_bar_and(NB_EPI_R, EPI_N, ok)) {
+            if (role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N,
+                          [&] { return nchunks == 0 || bwait(st_done, nchunks - 1, abort_f); })) {
                 tc_fence_after();
                 float *So = a.S_out + (size_t)unit * D * D + j;
 #pragma unroll 1
@@ -542,7 +562,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % NR, qs = c % QS;
             const int n = min(C, L - c * C);
-            if (!named_bar_and(NB_PREP_R, PREP_N, bwait(g_full, c, abort_f))) { give_up(); break; }
+            if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] { return bwait(g_full, c, abort_f); })) {
+                give_up();
+                break;
+            }
             // 1. log-gates and the quarter's prefix sums (base 2); tokens past
             //    the end of the sequence get no decay.
             float2 cs[16];
@@ -573,8 +596,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int qq = 0; qq < 4; ++qq)
                 if (qq < hq) { pre.x += T[qq].x; pre.y += T[qq].y; }
             if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[c & 1] = 1;
-            const bool ok_in = bwait(&k_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
-            if (!named_bar_and(NB_PREP_R, PREP_N, ok_in)) { give_up(); break; }
+            if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
+                    return bwait(&k_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
+                })) { give_up(); break; }
             const bool unsafe = unsafe_f[c & 1] != 0;
             const uint8_t *kraw = sm + SM::KV + s * SLOT + kblk * KB_K;
             const uint8_t *qraw = sm + SM::Q + qs * 2 * KB_T + kblk * KB_T;
@@ -583,9 +607,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // b_t - r for this thread's tokens: cs + (pre - half0)
                 const float2 o = make_float2(pre.x - half0.x, pre.y - half0.y);
                 const float2 F = make_float2(ex2(half1.x), ex2(half1.y));  // 2^{b_last - r}
-                const bool ok = c == 0 || (bwait(kr_free, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f) &&
-                                           bwait(kl_free, c - 1, abort_f));
-                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+                if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
+                        return c == 0 || (bwait(kr_free, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f) &&
+                                          bwait(kl_free, c - 1, abort_f));
+                    })) { give_up(); break; }
                 uint8_t *kr_t = sm + SM::KR + kblk * KB_T, *qr_t = sm + SM::QR + kblk * KB_T;
                 uint8_t *kl_t = sm + SM::KL + kblk * KB_T;
 #pragma unroll
@@ -608,10 +633,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 // Exact intra-chunk scores on the CUDA cores.  Scratch: the
                 // KL and W tiles hold b (fp32, [64][128]) meanwhile.
-                bool ok = (c == 0 || (bwait(kl_free, c - 1, abort_f) && bwait(w_free, c - 1, abort_f) &&
-                                      bwait(sc_free, c - 1, abort_f) && bwait(kr_free, c - 1, abort_f) &&
-                                      bwait(qr_free, c - 1, abort_f)));
-                if (!named_bar_and(NB_PREP_R, PREP_N, ok)) { give_up(); break; }
+                if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
+                        return c == 0 || (bwait(kl_free, c - 1, abort_f) && bwait(w_free, c - 1, abort_f) &&
+                                          bwait(sc_free, c - 1, abort_f) && bwait(kr_free, c - 1, abort_f) &&
+                                          bwait(qr_free, c - 1, abort_f));
+                    })) { give_up(); break; }
                 float *bz = reinterpret_cast<float *>(sm + SM::KL);
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt)
@@ -700,11 +726,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tl = tmem + tlane(quarter);
         const int st_ = tid - W_SOFT * 32;
         for (int c = 0; c < nchunks; ++c) {
-            const int c0 = c * C, n = min(C, L - c0), tg = c0 + t;
+            const int c0 = c * C, n = min(C, L - c0);
             const bool rowok = t < n;
             const int pbase = c0 - 64 * NP;  // global position of band column 0
-            bool ok = bwait(sc_full, c, abort_f) && bwait(a_full, c, abort_f);
-            if (!named_bar_and(NB_SOFT_R, SOFT_N, ok)) { give_up(); break; }
+            // Keys of row t: positions max(0, tg - w + 1) .. tg, i.e. band
+            // columns lo .. hi.
+            const int hi = t + 64 * NP, lo = max(-pbase, hi - w + 1);
+            const int d0 = 16 * hs - lo;
+            const uint32_t span = (uint32_t)(hi - lo);
+            if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
+                           [&] { return bwait(sc_full, c, abort_f) && bwait(a_full, c, abort_f); })) {
+                give_up();
+                break;
+            }
             tc_fence_after();
             // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
             float x[2 * NB][16];
@@ -720,8 +754,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int jj = 0; jj < 2 * NB; ++jj)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const int pp = pbase + 32 * jj + 16 * hs + e;
-                        const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
+                        // band column 32 jj + 16 hs + e is a key of this row iff lo <= col <= hi
+                        const bool valid = (uint32_t)(d0 + 32 * jj + e) <= span;
                         x[jj][e] = valid ? __uint_as_float(r[jj][e]) : -INFINITY;
                         mx = fmaxf(mx, x[jj][e]);
                     }
@@ -746,8 +780,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
             const float inv = a.alpha / sum;
-            ok = c == 0 || bwait(w_free, c - 1, abort_f);
-            if (!named_bar_and(NB_SOFT_R, SOFT_N, ok)) { give_up(); break; }
+            if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
+                           [&] { return c == 0 || bwait(w_free, c - 1, abort_f); })) {
+                give_up();
+                break;
+            }
             uint32_t ra2[2][16];  // intra-chunk scores of this thread's current-chunk columns
             tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
             tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);

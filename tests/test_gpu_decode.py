@@ -126,3 +126,31 @@ def test_decode_reports_a_position_outside_the_valid_range():
     assert rel_l2(y[seq], y_ref) <= 1e-2
     pos = st.pos.cpu()
     assert int(pos[0]) == wl.L + 1 and int(pos[2]) == wl.L + 1
+
+
+def test_long_context_prefill_then_decode_sampled_heads():
+    """B1 H32 L65536 d128 bf16, g ~ N(4,1), w64 m4: prefill of L tokens
+    (one launch), its state handed to 128 decode steps.  The oracle runs
+    the recurrence over all L + 128 tokens for sampled heads; both the
+    prefill rows and every decode step must match it (rel L2 <= 1e-2)."""
+    wl = WORKLOADS["long_context"]
+    n = wl.decode_steps
+    inp = prefill_inputs(wl, L=wl.L + n)
+    heads = [0, 21]
+    head = {k: (v[:, :, :wl.L].contiguous() if isinstance(v, torch.Tensor) and k != "mu" else v)
+            for k, v in inp.items()}
+    y_pre, st = gpu_prefill(head, wl.w)
+    ys = []
+    for t in range(wl.L, wl.L + n):
+        step = {k: inp[k][:, :, t].contiguous() for k in ("q", "k", "v", "g")}
+        ys.append(gpu_decode_step(step, inp["mu"], inp["alpha"], st).cpu())
+    y_dec = torch.stack(ys, dim=2)  # [B, H, n, d]
+    y_ref = O.forward_units_parallel(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], wl.w,
+                                     [(0, h) for h in heads])
+    got_pre = torch.stack([y_pre[0, h] for h in heads])
+    err_pre = rel_l2(got_pre, y_ref[:, :wl.L])
+    assert err_pre <= 1e-2, f"prefill rows: rel L2 {err_pre:.3e}"
+    got_dec = torch.stack([y_dec[0, h] for h in heads])
+    err_dec = rel_l2(got_dec, y_ref[:, wl.L:])
+    assert err_dec <= 1e-2, f"decode rows: rel L2 {err_dec:.3e}"
+    assert int(st.pos.cpu()[0]) == wl.L + n
