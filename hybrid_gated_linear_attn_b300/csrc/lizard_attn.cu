@@ -16,6 +16,7 @@
 #include "prefill_simt.cuh"
 #include "prefill_tc.cuh"
 #include "prefill_ws.cuh"
+#include "prefill_state.cuh"
 
 namespace lizard {
 
@@ -122,30 +123,99 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
 
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                          const CUtensorMap &tg, const ws::WsArgs &wa, int units, cudaStream_t s)
+                                          const CUtensorMap &tg, const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
     auto kern = ws::prefill_ws_kernel<NP>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<units, ws::THREADS, smem, s>>>(tq, tk, tv, tg, wa);
+    kern<<<ctas, ws::THREADS, smem, s>>>(tq, tk, tv, tg, wa);
     return launch_status();
 }
 
-// Warp-specialised tensor-core prefill (bf16, d = 128, w <= 65).
-static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s)
+static int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+// Sequence segments per (batch, head) unit: enough CTAs to cover the SMs
+// when there are few units, each segment at least 8 chunks long.
+static int prefill_segments(int units, int nchunks)
+{
+    const int p = sm_count() / (units > 0 ? units : 1);
+    const int cap = nchunks / 8;
+    return p < 1 || cap < 1 ? 1 : (p < cap ? p : cap);
+}
+
+// Bytes of scratch a segmented prefill needs: the segment states and decays.
+static size_t segment_scratch_bytes(int units, int nseg)
+{
+    return (size_t)units * (nseg - 1) * ((size_t)ws::D * ws::D + ws::D) * sizeof(float);
+}
+
+// The segment pre-pass: end state and total decay of every segment but the
+// last, then the start state of every segment (written over the end states).
+static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tg,
+                                           float *scratch, int units, int L, int seg_chunks, int nseg, cudaStream_t s)
+{
+    seg::SegArgs sa{scratch, scratch + (size_t)units * (nseg - 1) * ws::D * ws::D, L, seg_chunks, nseg};
+    if (cudaFuncSetAttribute(seg::segment_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)seg::SMEM_BYTES) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    seg::segment_state_kernel<<<units * (nseg - 1), seg::THREADS, seg::SMEM_BYTES, s>>>(tk, tv, tg, sa);
+    if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
+    seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, units, nseg);
+    return launch_status();
+}
+
+// Warp-specialised tensor-core prefill (bf16, d = 128, w <= 65).  With few
+// (batch, head) units and a long prompt the sequence is split into segments
+// that run side by side, after a pre-pass that computes every segment's
+// start state; `scratch` (nullable) holds those states, else they live in
+// stream-ordered temporary memory (cudaMallocAsync / cudaFreeAsync on `s`).
+static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, float *scratch = nullptr,
+                                       size_t scratch_bytes = 0, int force_segments = 0)
 {
     const int units = pa.B * pa.H;
+    const int nchunks = (pa.L + ws::C - 1) / ws::C;
+    int nseg = force_segments > 0 ? force_segments : prefill_segments(units, nchunks);
+    if (nseg > nchunks) nseg = nchunks;
+    const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
+    nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
+    if (nseg < 1) nseg = 1;
     CUtensorMap tq, tk, tv, tg;
     if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
         !make_token_map(&tv, pa.v, units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
         return LIZARD_ERR_CUDA;
+    float *seg_states = nullptr;
+    bool owned = false;
+    if (nseg > 1) {
+        const size_t need = segment_scratch_bytes(units, nseg);
+        if (scratch) {
+            if (scratch_bytes < need) return LIZARD_ERR_UNSUPPORTED;
+            seg_states = scratch;
+        } else if (cudaMallocAsync(reinterpret_cast<void **>(&seg_states), need, s) == cudaSuccess) {
+            owned = true;
+        } else {
+            cudaGetLastError();
+            nseg = 1;  // no scratch to be had: one CTA per unit walks the whole prompt
+        }
+    }
+    lizard_status rc = LIZARD_OK;
+    if (nseg > 1) rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, s);
     ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
-                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m};
-    return pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units, s)
-                     : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units, s);
+                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
+                  nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg};
+    if (rc == LIZARD_OK)
+        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units * nseg, s)
+                       : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units * nseg, s);
+    if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
+    return rc;
 }
 
 template <typename T, int D>

@@ -105,6 +105,11 @@ struct WsArgs {
     int64_t *pos;
     float alpha;
     int H, L, w, m;
+    // Sequence segments: CTA (unit, seg) covers chunks [seg*seg_chunks,
+    // (seg+1)*seg_chunks) and starts from S_init[unit][seg-1] (row = key
+    // dim), the state after the earlier segments; segment 0 starts from 0.
+    const float *S_init;
+    int seg_chunks, nseg;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -274,9 +279,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM::TSLOT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x, h = unit % a.H;
+    const int nseg = a.nseg;
+    const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, h = unit % a.H;
     const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
+    // This CTA's chunks, and the first chunk it loads: the band of its first
+    // chunk reaches NP chunks back into the previous segment.
+    const int c_begin = seg * a.seg_chunks, c_end = min(nchunks, c_begin + a.seg_chunks);
+    const int c_lo = c_begin > 0 ? c_begin - NP : 0;
+    const bool last_seg = seg == nseg - 1;
 
     // ---------------------------------------------------------- set-up
     if (warp == W_MMA) {
@@ -332,26 +343,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {}, g_issued = 0;
-            for (int c = 0; c < nchunks && !failed; ++c) {
-                if (c >= 1 && !bwait(g_empty, c - 1, abort_f)) { give_up(); break; }
-                mbar_arrive_expect_tx(g_full, 2 * KB_T);
-                tma_load_3d(sm + SM::G, &tg, g_full, 0, c * C, unit);
-                tma_load_3d(sm + SM::G + KB_T, &tg, g_full, 64, c * C, unit);
-                ++g_issued;
-                const int s = c % NR;
+            // keys and values of the band chunks before this segment
+            for (int c = c_lo; c < c_begin; ++c) {
+                const int s = (c - c_lo) % NR;
                 uint8_t *base = sm + SM::KV + s * SLOT;
-                if (c >= NR && !bwait(&k_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
                 tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
                 tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
                 ++k_issued[s];
-                const int qs = c % QS;
-                if (c >= QS && !bwait(&q_empty[qs], c / QS - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
+                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
+                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                ++v_issued[s];
+            }
+            for (int c = c_begin; c < c_end && !failed; ++c) {
+                const int pc = c - c_begin, r = c - c_lo;
+                if (pc >= 1 && !bwait(g_empty, pc - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(g_full, 2 * KB_T);
+                tma_load_3d(sm + SM::G, &tg, g_full, 0, c * C, unit);
+                tma_load_3d(sm + SM::G + KB_T, &tg, g_full, 64, c * C, unit);
+                ++g_issued;
+                const int s = r % NR;
+                uint8_t *base = sm + SM::KV + s * SLOT;
+                if (r >= NR && !bwait(&k_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
+                mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
+                tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
+                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                ++k_issued[s];
+                const int qs = pc % QS;
+                if (pc >= QS && !bwait(&q_empty[qs], pc / QS - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&q_full[qs], 2 * KB_T);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T, &tq, &q_full[qs], 0, c * C, unit);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T + KB_T, &tq, &q_full[qs], 64, c * C, unit);
                 ++q_issued[qs];
-                if (c >= NR && !bwait(&v_empty[s], c / NR - 1, abort_f)) { give_up(); break; }
+                if (r >= NR && !bwait(&v_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
                 tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
                 tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
@@ -374,18 +399,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t id_sc_cur = instr_desc(64, 64 + META_ROWS, FMT_BF16, 0, 0);
             const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
             const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % NR, qs = c % QS;
+            for (int c = c_begin; c < c_end; ++c) {
+                const int pc = c - c_begin, r = c - c_lo;
+                const int s = r % NR, qs = pc % QS;
                 const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
-                if (!bwait(&k_full[s], c / NR, abort_f) || !bwait(&q_full[qs], c / QS, abort_f) ||
-                    (c >= 1 && !bwait(sc_free, c - 1, abort_f))) { give_up(); break; }
+                if ((pc == 0 && c_lo < c_begin && !bwait(&k_full[0], 0, abort_f)) ||
+                    !bwait(&k_full[s], r / NR, abort_f) || !bwait(&q_full[qs], pc / QS, abort_f) ||
+                    (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
                 // window + meta logits
 #pragma unroll
                 for (int j = 0; j <= NP; ++j) {
                     const int cj = c - NP + j;
-                    if (cj < 0) continue;
-                    const uint32_t kb = sb + SM::KV + (cj % NR) * SLOT;
+                    if (cj < c_lo) continue;
+                    const uint32_t kb = sb + SM::KV + ((cj - c_lo) % NR) * SLOT;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16_ss(tmem + T_SC + 64 * j, smem_desc(qb + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
@@ -395,9 +422,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_commit(sc_full);
                 mma_commit(&q_empty[qs]);
                 // intra-chunk decayed scores
-                if (!bwait(prep_ready, c, abort_f)) { give_up(); break; }
+                if (!bwait(prep_ready, pc, abort_f)) { give_up(); break; }
                 tc_fence_after();
-                if (!unsafe_f[c & 1]) {
+                if (!unsafe_f[pc & 1]) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16_ss(tmem + TM::A, smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
@@ -408,9 +435,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // The key tile of chunk c - NP has no reader left: the last
                 // band scores that use it were issued above, and its raw keys
                 // were read by the prep of chunk c - NP (done: prep_ready).
-                if (c - NP >= 0) mma_commit(&k_empty[(c - NP) % NR]);
+                if (c - NP >= c_lo) mma_commit(&k_empty[(c - NP - c_lo) % NR]);
                 // S^T += V^T KL (S^T decayed by the state pass)
-                if (!bwait(s_ready, c, abort_f) || !bwait(&v_full[s], c / NR, abort_f)) { give_up(); break; }
+                if (!bwait(s_ready, pc, abort_f) || !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
                 tc_fence_after();
                 {
                     const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V;
@@ -432,10 +459,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint32_t id_y1 = instr_desc(128, 64, FMT_BF16, 0, 0);
             const uint32_t id_y2 = instr_desc(128, 64, FMT_BF16, 1, 0);
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
+                const int pc = c - c_begin, r = c - c_lo;
                 // y^T = S16 QR^T (inter-chunk readout)
-                if (!bwait(prep_ready, c, abort_f) || !bwait(s_ready, c, abort_f) ||
-                    (c >= 1 && !bwait(y_free, c - 1, abort_f))) { give_up(); break; }
+                if (!bwait(prep_ready, pc, abort_f) || !bwait(s_ready, pc, abort_f) ||
+                    (pc >= 1 && !bwait(y_free, pc - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
@@ -443,14 +471,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
                 mma_commit(qr_free);
                 // y^T += V_band^T W^T
-                if (!bwait(w_full, c, abort_f) || !bwait(&v_full[c % NR], c / NR, abort_f) ||
-                    (NP == 0 && !bwait(st_done, c, abort_f))) { give_up(); break; }
+                if (!bwait(w_full, pc, abort_f) || !bwait(&v_full[r % NR], r / NR, abort_f) ||
+                    (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f)) ||
+                    (NP == 0 && !bwait(st_done, pc, abort_f))) { give_up(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j <= NP; ++j) {
                     const int cj = c - NP + j;
-                    if (cj < 0) continue;
-                    const uint32_t vb = sb + SM::KV + (cj % NR) * SLOT + SLOT_V;
+                    if (cj < c_lo) continue;
+                    const uint32_t vb = sb + SM::KV + ((cj - c_lo) % NR) * SLOT + SLOT_V;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ss(tmem + T_Y, smem_desc(vb + kk * 2048, KB_T, 1024),
@@ -461,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // The value tile of chunk c - NP has no reader left: its state
                 // update (issued before A_c, which the softmax waited for;
                 // for NP = 0 st_done above) and these products.
-                if (c - NP >= 0) mma_commit(&v_empty[(c - NP) % NR]);
+                if (c - NP >= c_lo) mma_commit(&v_empty[(c - NP - c_lo) % NR]);
             }
             mma_commit(drain_y);
             bwait(drain_y, 0, abort_f);
@@ -473,22 +502,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int j = 32 * quarter + lane;  // value dim = tensor-memory lane
         const uint32_t tl = tmem + tlane(quarter);
         {
-            uint32_t z[16];
+            // Initial state: zero, or the state after the earlier segments.
+            const float *Si = (seg > 0 && a.S_init) ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * D * D + j
+                                                    : nullptr;
+#pragma unroll 1
+            for (int cc = 0; cc < D; cc += 16) {
+                uint32_t z[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) z[e] = 0u;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 16) tmem_st16(tl + T_S + cc, z);
+                for (int e = 0; e < 16; ++e) z[e] = Si ? __float_as_uint(Si[(size_t)(cc + e) * D]) : 0u;
+                tmem_st16(tl + T_S + cc, z);
+            }
             tmem_wait_st();
         }
         const int et = tid - W_EPI * 32;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
+            const int pc = c - c_begin;
             const int c0 = c * C, n = min(C, L - c0);
             if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] {
-                    return (c == 0 || (bwait(st_done, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f))) &&
-                           bwait(prep_ready, c, abort_f);
+                    return (pc == 0 || (bwait(st_done, pc - 1, abort_f) && bwait(qr_free, pc - 1, abort_f))) &&
+                           bwait(prep_ready, pc, abort_f);
                 })) { give_up(); break; }
             tc_fence_after();
-            const float *dv = dec_v + (c & 1) * 128, *ev = er_v + (c & 1) * 128;
+            const float *dv = dec_v + (pc & 1) * 128, *ev = er_v + (pc & 1) * 128;
 #pragma unroll 1
             for (int cb = 0; cb < D; cb += 32) {
                 uint32_t r0[16], r1[16];
@@ -517,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             named_bar(NB_EPI, EPI_N);
             if (et == 0) mbar_arrive(s_ready);
             // epilogue: y rows of this chunk
-            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] { return bwait(y_full, c, abort_f); })) {
+            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] { return bwait(y_full, pc, abort_f); })) {
                 give_up();
                 break;
             }
@@ -537,9 +572,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (et == 0) mbar_arrive(y_free);
         }
         // Final state S (row i = key dim): S^T[j][i] -> S_out[i][j].
-        if (!failed && a.S_out) {
+        if (!failed && a.S_out && last_seg) {
             if (role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N,
-                          [&] { return nchunks == 0 || bwait(st_done, nchunks - 1, abort_f); })) {
+                          [&] { return c_end == c_begin || bwait(st_done, c_end - c_begin - 1, abort_f); })) {
                 tc_fence_after();
                 float *So = a.S_out + (size_t)unit * D * D + j;
 #pragma unroll 1
@@ -559,10 +594,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int tp = tid - W_PREP * 32;
         const int p = tp & 63, hq = tp >> 6;       // key dims 2p, 2p+1; tokens 16 hq .. 16 hq + 15
         const uint32_t kblk = (p / 32), kbyte = (p % 32) * 4;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % NR, qs = c % QS;
+        for (int c = c_begin; c < c_end; ++c) {
+            const int pc = c - c_begin, r = c - c_lo;
+            const int s = r % NR, qs = pc % QS;
             const int n = min(C, L - c * C);
-            if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] { return bwait(g_full, c, abort_f); })) {
+            if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] { return bwait(g_full, pc, abort_f); })) {
                 give_up();
                 break;
             }
@@ -595,11 +631,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
                 if (qq < hq) { pre.x += T[qq].x; pre.y += T[qq].y; }
-            if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[c & 1] = 1;
+            if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[pc & 1] = 1;
             if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                    return bwait(&k_full[s], c / NR, abort_f) && bwait(&q_full[qs], c / QS, abort_f);
+                    return bwait(&k_full[s], r / NR, abort_f) && bwait(&q_full[qs], pc / QS, abort_f);
                 })) { give_up(); break; }
-            const bool unsafe = unsafe_f[c & 1] != 0;
+            const bool unsafe = unsafe_f[pc & 1] != 0;
             const uint8_t *kraw = sm + SM::KV + s * SLOT + kblk * KB_K;
             const uint8_t *qraw = sm + SM::Q + qs * 2 * KB_T + kblk * KB_T;
             const float2 blast = make_float2(half0.x + half1.x, half0.y + half1.y);
@@ -608,8 +644,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float2 o = make_float2(pre.x - half0.x, pre.y - half0.y);
                 const float2 F = make_float2(ex2(half1.x), ex2(half1.y));  // 2^{b_last - r}
                 if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                        return c == 0 || (bwait(kr_free, c - 1, abort_f) && bwait(qr_free, c - 1, abort_f) &&
-                                          bwait(kl_free, c - 1, abort_f));
+                        return pc == 0 || (bwait(kr_free, pc - 1, abort_f) && bwait(qr_free, pc - 1, abort_f) &&
+                                          bwait(kl_free, pc - 1, abort_f));
                     })) { give_up(); break; }
                 uint8_t *kr_t = sm + SM::KR + kblk * KB_T, *qr_t = sm + SM::QR + kblk * KB_T;
                 uint8_t *kl_t = sm + SM::KL + kblk * KB_T;
@@ -627,16 +663,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<uint32_t *>(kl_t + off) = f2_to_bf2(kl.x, kl.y);
                 }
                 if (hq == 0) {
-                    er_v[(c & 1) * 128 + 2 * p] = ex2(half0.x);
-                    er_v[(c & 1) * 128 + 2 * p + 1] = ex2(half0.y);
+                    er_v[(pc & 1) * 128 + 2 * p] = ex2(half0.x);
+                    er_v[(pc & 1) * 128 + 2 * p + 1] = ex2(half0.y);
                 }
             } else {
                 // Exact intra-chunk scores on the CUDA cores.  Scratch: the
                 // KL and W tiles hold b (fp32, [64][128]) meanwhile.
                 if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                        return c == 0 || (bwait(kl_free, c - 1, abort_f) && bwait(w_free, c - 1, abort_f) &&
-                                          bwait(sc_free, c - 1, abort_f) && bwait(kr_free, c - 1, abort_f) &&
-                                          bwait(qr_free, c - 1, abort_f));
+                        return pc == 0 || (bwait(kl_free, pc - 1, abort_f) && bwait(w_free, pc - 1, abort_f) &&
+                                          bwait(sc_free, pc - 1, abort_f) && bwait(kr_free, pc - 1, abort_f) &&
+                                          bwait(qr_free, pc - 1, abort_f));
                     })) { give_up(); break; }
                 float *bz = reinterpret_cast<float *>(sm + SM::KL);
 #pragma unroll
@@ -688,25 +724,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                         f2_to_bf2(kv.x * ex2(blast.x - bt.x), kv.y * ex2(blast.y - bt.y));
                 }
                 if (hq == 0) {
-                    er_v[(c & 1) * 128 + 2 * p] = 1.f;
-                    er_v[(c & 1) * 128 + 2 * p + 1] = 1.f;
+                    er_v[(pc & 1) * 128 + 2 * p] = 1.f;
+                    er_v[(pc & 1) * 128 + 2 * p + 1] = 1.f;
                 }
             }
             if (hq == 0) {
-                dec_v[(c & 1) * 128 + 2 * p] = ex2(blast.x);
-                dec_v[(c & 1) * 128 + 2 * p + 1] = ex2(blast.y);
+                dec_v[(pc & 1) * 128 + 2 * p] = ex2(blast.x);
+                dec_v[(pc & 1) * 128 + 2 * p + 1] = ex2(blast.y);
             }
             fence_proxy_async_smem();
             named_bar(NB_PREP, PREP_N);
             if (tp == 0) {
-                unsafe_f[(c + 1) & 1] = 0;  // the MMA issuer read it for chunk c - 1 before state_{c-1}
+                unsafe_f[(pc + 1) & 1] = 0;  // the MMA issuer read it for chunk c - 1 before state_{c-1}
                 mbar_arrive(prep_ready);
                 if (!unsafe) mbar_arrive(a_full);
                 mbar_arrive(&q_empty[qs]);
             }
         }
         // State hand-off: the last min(L, w) keys and values into the ring, pos = L.
-        if (!failed && a.S_out) {
+        if (!failed && a.S_out && last_seg) {
             const int first = max(0, L - w);
             const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
             __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
@@ -725,7 +761,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int t = 16 * quarter + (lane & 15);
         const uint32_t tl = tmem + tlane(quarter);
         const int st_ = tid - W_SOFT * 32;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
+            const int pc = c - c_begin;
             const int c0 = c * C, n = min(C, L - c0);
             const bool rowok = t < n;
             const int pbase = c0 - 64 * NP;  // global position of band column 0
@@ -735,7 +772,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int d0 = 16 * hs - lo;
             const uint32_t span = (uint32_t)(hi - lo);
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
-                           [&] { return bwait(sc_full, c, abort_f) && bwait(a_full, c, abort_f); })) {
+                           [&] { return bwait(sc_full, pc, abort_f) && bwait(a_full, pc, abort_f); })) {
                 give_up();
                 break;
             }
@@ -781,7 +818,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
             const float inv = a.alpha / sum;
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
-                           [&] { return c == 0 || bwait(w_free, c - 1, abort_f); })) {
+                           [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
                 give_up();
                 break;
             }

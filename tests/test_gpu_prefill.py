@@ -62,6 +62,14 @@ CASES = [
     ("window_66", "bf16", 1, 2, 333, 128, 66, 4, 3.0, 1.0, 1.0),
     ("one_chunk_exact", "bf16", 2, 2, 64, 128, 64, 4, 3.0, 1.0, 1.0),
     ("alpha_zero", "bf16", 1, 2, 190, 128, 64, 4, 3.0, 1.0, 0.0),
+    # few (batch, head) units and long prompts: the prompt runs as sequence
+    # segments after a pre-pass for the segments' start states
+    ("segments_2", "bf16", 1, 2, 1000, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("segments_5_ragged", "bf16", 1, 2, 3000, 128, 48, 4, 3.0, 1.0, 0.7),
+    ("segments_strong_decay", "bf16", 1, 2, 2000, 128, 64, 4, 0.0, 2.0, 0.5),
+    ("segments_exact_intra", "bf16", 1, 1, 1500, 128, 32, 2, -8.0, 4.0, 1.0),
+    ("segments_window_one", "bf16", 1, 2, 1200, 128, 1, 3, 3.0, 1.0, 1.0),
+    ("segments_open_gates_no_meta", "bf16", 1, 1, 2500, 128, 64, 0, 12.0, 0.5, 1.0),
 ]
 
 
