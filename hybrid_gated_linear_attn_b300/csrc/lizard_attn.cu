@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/lizard_attn.h"
 #include "common.cuh"
@@ -230,6 +231,32 @@ static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
     return launch_status();
 }
 
+// ---------------------------------------------------------------- allocation-free prefill
+// Segment states of lizard_attn_prefill_noalloc: a fixed array in device
+// memory, held by every GPU that loads this library until the process ends.
+constexpr size_t NOALLOC_FLOATS = LIZARD_NOALLOC_SCRATCH_BYTES / sizeof(float);
+static __device__ __align__(256) float g_prefill_scratch[NOALLOC_FLOATS];
+
+// The array's device address on the current device.  In host code the name
+// g_prefill_scratch is a host-side stand-in, not a device address, so it is
+// looked up once per device (cudaGetSymbolAddress) with that device current.
+static lizard_status noalloc_scratch(float **out)
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static float *addr[MAX_DEV] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return LIZARD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || !p) return LIZARD_ERR_CUDA;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *out = addr[dev];
+    return LIZARD_OK;
+}
+
 }  // namespace lizard
 
 using namespace lizard;
@@ -294,6 +321,39 @@ lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, c
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
                          : launch_prefill<__nv_bfloat16, 64>(pa, s);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
+}
+
+lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                          const void *meta_k, float alpha, int B, int H, int L, int dk, int dv, int w,
+                                          int m, lizard_dtype dtype, void *y, const lizard_state *st,
+                                          lizard_stream_t stream)
+{
+    if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
+    if (B < 0 || H < 1 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0) return LIZARD_ERR_INVALID_ARG;
+    if (L > 0 && (!q || !k || !v || !g || !y)) return LIZARD_ERR_INVALID_ARG;
+    if (m > 0 && !meta_k) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(y) ||
+        (m > 0 && !aligned16(meta_k)))
+        return LIZARD_ERR_INVALID_ARG;
+    // The variant covers the tensor-core prefill, the one with scratch.
+    if (dtype != LIZARD_BF16 || dk != 128 || dv != 128 || w > 65 || m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
+    if (st) {
+        lizard_status rc = check_state(st);
+        if (rc != LIZARD_OK) return rc;
+        if (st->B != B || st->H != H || st->dk != dk || st->dv != dv || st->w != w || st->dtype != dtype)
+            return LIZARD_ERR_INVALID_ARG;
+    }
+    if (B == 0) return LIZARD_OK;
+    if (L == 0) return st ? lizard_state_init(st, stream) : LIZARD_OK;
+    float *scratch = nullptr;
+    lizard_status rc = noalloc_scratch(&scratch);
+    if (rc != LIZARD_OK) return rc;
+    PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m,
+                   st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
+                   st ? st->pos : nullptr};
+    // Segment states beyond LIZARD_NOALLOC_SCRATCH_BYTES: LIZARD_ERR_UNSUPPORTED, nothing launched.
+    return launch_prefill_ws(pa, (cudaStream_t)stream, scratch, LIZARD_NOALLOC_SCRATCH_BYTES);
 }
 
 lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,

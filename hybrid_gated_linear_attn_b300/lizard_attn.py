@@ -23,7 +23,7 @@ LIZARD_F32, LIZARD_BF16 = 0, 1
 LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
-EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_decode_step",
+EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_noalloc", "lizard_attn_decode_step",
            "lizard_check_device_status", "lizard_status_string")
 
 
@@ -59,6 +59,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lizard_state_init.restype = I
         lib.lizard_attn_prefill.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
         lib.lizard_attn_prefill.restype = I
+        lib.lizard_attn_prefill_noalloc.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
+        lib.lizard_attn_prefill_noalloc.restype = I
         lib.lizard_attn_decode_step.argtypes = [P, P, P, P, P, F, I, P, SP, P]
         lib.lizard_attn_decode_step.restype = I
         lib.lizard_check_device_status.argtypes = [P]
@@ -139,6 +141,25 @@ def lizard_attn_prefill(q, k, v, g, meta_k, alpha, w, y=None, state: LizardState
         B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(y),
         ctypes.byref(st) if st is not None else None, _stream(stream))
     _check(rc, "lizard_attn_prefill")
+    return y
+
+
+def lizard_attn_prefill_noalloc(q, k, v, g, meta_k, alpha, w, y=None, state: LizardState | None = None,
+                                stream=None) -> torch.Tensor:
+    """lizard_attn_prefill without device allocation inside the call (bf16,
+    d = 128, w <= 65): segment states go to the library's fixed device array.
+    ``y`` is allocated here when not given; pass it to allocate nothing."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    m = meta_k.shape[1] if meta_k is not None else 0
+    if y is None:
+        y = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    st = state.c_struct() if state is not None else None
+    rc = library().lizard_attn_prefill_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha),
+        B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(y),
+        ctypes.byref(st) if st is not None else None, _stream(stream))
+    _check(rc, "lizard_attn_prefill_noalloc")
     return y
 
 

@@ -116,6 +116,38 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
                                   lizard_stream_t stream);
 
 /*
+ * lizard_attn_prefill_noalloc: lizard_attn_prefill for callers that must not
+ * allocate device memory during a call -- for example a serving runtime
+ * that reserves all device memory up front for its own pool, code that must
+ * not touch the driver's allocator while other work is being captured or
+ * timed, or an embedding that forbids run-time allocation.  (The paper has
+ * no counterpart; this entry point is about memory management only.)
+ *
+ * Same arguments and results as lizard_attn_prefill; it covers the
+ * tensor-core path (bf16, dk == dv == 128, w <= 65), LIZARD_ERR_UNSUPPORTED
+ * otherwise.  When a prompt runs as sequence segments (few batch x head
+ * units, long L) the segments' start states need scratch.  This variant
+ * keeps it in a fixed device array of LIZARD_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * that every GPU loading the library holds until the process exits, and
+ * calls no cudaMalloc, cudaFree or allocating library routine.  A problem
+ * whose segment states would not fit (units x (segments - 1) x 66048 bytes)
+ * is rejected with LIZARD_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on that device.
+ *   - Every call shares the one array and overwrites what it reads (nothing
+ *     in it needs to start at zero), so calls whose work overlaps on the GPU
+ *     -- on different streams, or from different host threads -- race and
+ *     must be serialised by the caller.
+ */
+#define LIZARD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+LIZARD_API lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                          const void *meta_k, float alpha,
+                                          int B, int H, int L, int dk, int dv, int w, int m,
+                                          lizard_dtype dtype, void *y, const lizard_state *st,
+                                          lizard_stream_t stream);
+
+/*
  * lizard_attn_decode_step: one new token for each of st->B sequences and
  * st->H heads, continuing from `st` (updated in place).
  *   q, k, g  [B][H][dk]  st->dtype;  v [B][H][dv];  meta_k [H][m][dk]

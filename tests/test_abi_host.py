@@ -132,6 +132,6 @@ def test_state_init_rejects(lib):
 
 def test_binding_names_match_the_c_abi():
     import hybrid_gated_linear_attn_b300 as pkg
-    for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_decode_step",
-                 "lizard_check_device_status", "lizard_status_string"):
+    for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_noalloc",
+                 "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string"):
         assert callable(getattr(pkg, name))
