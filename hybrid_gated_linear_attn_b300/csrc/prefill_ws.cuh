@@ -181,19 +181,18 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
     return upk2(r);
 }
-// log2_sigmoid of a pair, the polynomial in packed arithmetic.
+// log2_sigmoid of a pair: min(g, 0) log2(e) - log2(1 + 2^{-|g| log2(e)}),
+// both transcendentals on the MUFU pipe (short dependency chain).
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float2 log2_sigmoid2(float2 g)
 {
-    const float2 u = make_float2(ex2(-fabsf(g.x) * LOG2E), ex2(-fabsf(g.y) * LOG2E));
-    float2 p = make_float2(0.015127916f, 0.015127916f);
-    p = fma2(p, u, make_float2(-0.078158207f, -0.078158207f));
-    p = fma2(p, u, make_float2(0.19238505f, 0.19238505f));
-    p = fma2(p, u, make_float2(-0.32461637f, -0.32461637f));
-    p = fma2(p, u, make_float2(0.47311336f, 0.47311336f));
-    p = fma2(p, u, make_float2(-0.72051549f, -0.72051549f));
-    p = fma2(p, u, make_float2(1.4426640f, 1.4426640f));
-    const float2 mn = make_float2(fminf(g.x, 0.f) * LOG2E, fminf(g.y, 0.f) * LOG2E);
-    return fma2(make_float2(-u.x, -u.y), p, mn);
+    const float ua = ex2(-fabsf(g.x) * LOG2E), ub = ex2(-fabsf(g.y) * LOG2E);
+    return make_float2(fminf(g.x, 0.f) * LOG2E - lg2(1.f + ua), fminf(g.y, 0.f) * LOG2E - lg2(1.f + ub));
 }
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
 {
