@@ -406,6 +406,8 @@ def run_profile_case(args):
     wl = WORKLOADS[args.workload]
     if args.batch:
         wl = wl.replace(B=args.batch)
+    if args.seq_len:
+        wl = wl.replace(L=args.seq_len)
     if args.profile_case == "prefill":
         inp = prefill_inputs(wl)
         q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
@@ -440,6 +442,7 @@ def main(argv=None):
                     help="only launch this operator W + K times (a small program for ncu); no JSON line")
     ap.add_argument("--workload", default=None, help="workload of --profile-case (default: the bench's)")
     ap.add_argument("--batch", type=int, default=0, help="batch override for --profile-case")
+    ap.add_argument("--seq-len", type=int, default=0, help="prompt length override for --profile-case prefill")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.profile_case:
