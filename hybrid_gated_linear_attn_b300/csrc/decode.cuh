@@ -144,6 +144,11 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
     float *stat = red + RG * DH;                // M, alpha / Z
     uint64_t *bar = reinterpret_cast<uint64_t *>(stat + 4);
 
+    // The next decode step may begin launching now; this one waits until the
+    // previous kernel on the stream has finished and its writes are visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // 1. Every load up front: the bulk copies (thread 0), this CTA's half of
     //    S into registers (all threads), the position.
     if (tid == 0) {

@@ -227,7 +227,20 @@ static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
     auto kern = decode_step_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.total) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<da.B * da.H * DECODE_SPLIT, DECODE_THREADS, plan.total, s>>>(da);
+    // Programmatic dependent launch: this step's CTAs may start while the
+    // previous kernel on the stream drains; the kernel waits for it
+    // (griddepcontrol.wait) before touching any data.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(da.B * da.H * DECODE_SPLIT));
+    cfg.blockDim = dim3(DECODE_THREADS);
+    cfg.dynamicSmemBytes = plan.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, da) != cudaSuccess) return LIZARD_ERR_CUDA;
     return launch_status();
 }
 
