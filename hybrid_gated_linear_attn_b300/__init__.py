@@ -7,6 +7,7 @@ from .lizard_attn import (  # noqa: F401
     LizardState,
     lizard_attn_decode_step,
     lizard_attn_prefill,
+    lizard_attn_prefill_continue,
     lizard_attn_prefill_noalloc,
     lizard_check_device_status,
     lizard_state_init,

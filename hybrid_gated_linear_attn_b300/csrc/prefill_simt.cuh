@@ -30,6 +30,14 @@ struct PrefillArgs {
     float *S_out;
     void *ring_k, *ring_v;
     int64_t *pos;
+    // Continuation of a sequence (all null / 0 for a prompt from the empty
+    // state): p0[b] is the position of sequence b's first new token, hist_k /
+    // hist_v [units][HR][d] the tokens before it (row HR - 1 = token p0 - 1;
+    // rows past min(p0, w - 1) are zero) and S0 [units][d][d] the start state.
+    const int64_t *p0;
+    const void *hist_k, *hist_v;
+    int HR;
+    const float *S0;
 };
 
 constexpr int SIMT_C = 64;        // chunk length
@@ -71,8 +79,14 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
     const T *g = static_cast<const T *>(a.g) + base;
     const T *mu = static_cast<const T *>(a.mu) + (size_t)h * m * D;
     T *y = static_cast<T *>(a.y) + base;
+    const T *hk = a.HR ? static_cast<const T *>(a.hist_k) + (size_t)unit * a.HR * D : nullptr;
+    const T *hv = a.HR ? static_cast<const T *>(a.hist_v) + (size_t)unit * a.HR * D : nullptr;
+    // Window keys before the prompt: tokens -nvalid .. -1 (hist row HR + tau).
+    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
+    const int nvalid = a.HR ? (int)min(p0, (int64_t)(w - 1)) : 0;
 
-    for (int i = tid; i < D * D; i += SIMT_THREADS) S_s[i] = 0.f;
+    const float *S0 = a.S0 ? a.S0 + (size_t)unit * D * D : nullptr;
+    for (int i = tid; i < D * D; i += SIMT_THREADS) S_s[i] = S0 ? S0[i] : 0.f;
 
     for (int c0 = 0; c0 < L; c0 += C) {
         const int n = min(C, L - c0);
@@ -125,9 +139,9 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
 #pragma unroll
                 for (int jj = 0; jj < JPL; ++jj) acc[jj] += as * v_s[s * D + lane + 32 * jj];
             }
-            // anchor: window tau in [max(0, t_g - w + 1), t_g] plus m sinks
+            // anchor: window tau in [max(-nvalid, t_g - w + 1), t_g] plus m sinks
             const int tg = c0 + t;
-            const int first = max(0, tg - w + 1);
+            const int first = max(-nvalid, tg - w + 1);
             const int nk = tg - first + 1;
             for (int c = 0; c < nk + m; ++c) {
                 float part = 0.f;
@@ -136,7 +150,8 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
                     if (tau >= c0) {
                         for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * k_s[(tau - c0) * LD + i];
                     } else {
-                        for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * to_f32(k[(size_t)tau * D + i]);
+                        const T *kr = tau >= 0 ? k + (size_t)tau * D : hk + (size_t)(a.HR + tau) * D;
+                        for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * to_f32(kr[i]);
                     }
                 } else {
                     for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * to_f32(mu[(size_t)(c - nk) * D + i]);
@@ -158,7 +173,9 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
 #pragma unroll
                 for (int jj = 0; jj < JPL; ++jj) {
                     const int j = lane + 32 * jj;
-                    const float vv = tau >= c0 ? v_s[(tau - c0) * D + j] : to_f32(v[(size_t)tau * D + j]);
+                    const float vv = tau >= c0 ? v_s[(tau - c0) * D + j]
+                                     : tau >= 0 ? to_f32(v[(size_t)tau * D + j])
+                                                : to_f32(hv[(size_t)(a.HR + tau) * D + j]);
                     acc[jj] += pc * vv;
                 }
             }
@@ -192,7 +209,8 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
         }
     }
     __syncthreads();
-    // 6. State out: S, the last min(L, w) tokens into the ring, pos = L.
+    // 6. State out: S, the last min(L, w) tokens into the ring (token p0 + tau
+    //    in slot (p0 + tau) % w), pos = p0 + L.
     if (a.S_out) {
         float *So = a.S_out + (size_t)unit * D * D;
         for (int i = tid; i < D * D; i += SIMT_THREADS) So[i] = S_s[i];
@@ -201,10 +219,11 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
         const int first = max(0, L - w);
         for (int e = tid; e < (L - first) * D; e += SIMT_THREADS) {
             const int tau = first + e / D, i = e % D;
-            rk[(size_t)(tau % w) * D + i] = k[(size_t)tau * D + i];
-            rv[(size_t)(tau % w) * D + i] = v[(size_t)tau * D + i];
+            const size_t slot = (size_t)((p0 + tau) % w);
+            rk[slot * D + i] = k[(size_t)tau * D + i];
+            rv[slot * D + i] = v[(size_t)tau * D + i];
         }
-        if (h == 0 && tid == 0) a.pos[unit / a.H] = L;
+        if (h == 0 && tid == 0) a.pos[unit / a.H] = p0 + L;
     }
 }
 

@@ -240,18 +240,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == W_MMA) tmem_dealloc(tmem, 128);
 }
 
-// Segment start states: S_start(0) = 0 and
+// Segment start states: S_start(0) = S0 (zero when S0 is null) and
 // S_start(p+1) = diag(2^{Lam_p}) S_start(p) + dS_p, written over dS_p, so
-// that dS[u][p] holds S_start(p + 1) afterwards.  One thread per state
-// element and unit.
-__global__ void segment_scan_kernel(float *dS, const float *lam, int units, int nseg)
+// that dS[u][p] holds S_start(p + 1) afterwards.  S0_copy (nullable)
+// receives a copy of S0 for the first segment, which must not read S0 in
+// place: the last segment writes the final state over it.  One thread per
+// state element and unit.
+__global__ void segment_scan_kernel(float *dS, const float *lam, int units, int nseg, const float *S0,
+                                    float *S0_copy)
 {
     const int nsp = nseg - 1;
     const int u = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;  // i * D + j
     if (u >= units || e >= D * D) return;
     const int i = e / D;
-    float S = 0.f;
+    float S = S0 ? S0[(size_t)u * D * D + e] : 0.f;
+    if (S0_copy) S0_copy[(size_t)u * D * D + e] = S;
     for (int q = 0; q < nsp; ++q) {
         const size_t off = ((size_t)u * nsp + q) * D * D + e;
         S = exp2f(lam[((size_t)u * nsp + q) * D + i]) * S + dS[off];

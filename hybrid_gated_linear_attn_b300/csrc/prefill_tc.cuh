@@ -87,6 +87,14 @@ struct TcArgs {
     int64_t *pos;
     float alpha;
     int H, L, w, m, nprev;
+    // Continuation of a sequence (null / 0 for a prompt from the empty
+    // state): p0[b] is the position of sequence b's first new token, S0
+    // [units][D][D] the start state, and HR (64 * nprev or 0) the rows of the
+    // window history loaded as chunks -nprev .. -1 (tensor maps thk, thv:
+    // row HR - 1 = token p0 - 1, rows past min(p0, w - 1) zero).
+    const int64_t *p0;
+    const float *S0;
+    int HR;
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -126,7 +134,8 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi)
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const TcArgs a)
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap thk,
+                      const __grid_constant__ CUtensorMap thv, const TcArgs a)
 {
     constexpr int NB = NP + 1;     // band chunks
     constexpr int PART = 16 * NB;  // band columns per softmax thread (four threads per row)
@@ -145,6 +154,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int unit = blockIdx.x, h = unit % a.H;
     const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
+    // Window history: NH chunks before the prompt (chunks -NH .. -1), of
+    // which tokens -nvalid .. -1 are keys.  Chunk c lives in k/v slot
+    // (c + NH) % NR.
+    const int NH = a.HR > 0 ? NP : 0;
+    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
+    const int nvalid = NH > 0 ? (int)min(p0, (int64_t)(w - 1)) : 0;
     // Prep mapping: key dims 2ip and 2ip+1, tokens 16*tqr .. 16*tqr+15.
     const int ip = tid & 63, tqr = tid >> 6;
     // Softmax mapping (M = 64 accumulator layout): row srow, column part 2*half + ssub.
@@ -160,6 +175,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        if (NH > 0) {
+            prefetch_tmap(&thk);
+            prefetch_tmap(&thv);
+        }
     }
     // Meta keys of this head, zero rows past m.
     for (int e = tid; e < META_ROWS * D; e += THREADS) {
@@ -171,11 +190,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (warp < 4) {  // S^T = 0
-        uint32_t z[16];
+    if (warp < 4) {  // S^T = S0^T (zero when not given)
+        const int j = 32 * quarter + lane;
+        const float *Si = a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr;
+        for (int c = 0; c < D; c += 16) {
+            uint32_t z[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0u;
-        for (int c = 0; c < D; c += 16) tmem_st16(tmem + tmem_lane(quarter) + T_ST + c, z);
+            for (int i = 0; i < 16; ++i) z[i] = Si ? __float_as_uint(Si[(size_t)(c + i) * D]) : 0u;
+            tmem_st16(tmem + tmem_lane(quarter) + T_ST + c, z);
+        }
         tmem_wait_st();
     }
 
@@ -201,17 +224,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sm + OFF_Q + TILE, &tq, bar_q, 64, c * C, unit);
         ++issued[B_Q];
     };
-    auto issue_kv = [&](int c) {
-        const int s = c % NR;
+    auto issue_kv = [&](int c) {  // c < 0: a chunk of the window history
+        const int s = (c + NH) % NR;
         uint8_t *base = sm + OFF_KV + s * KV_SLOT;
+        const CUtensorMap *mk = c < 0 ? &thk : &tk, *mv = c < 0 ? &thv : &tv;
+        const int row = c < 0 ? a.HR + c * C : c * C;
         mbar_arrive_expect_tx(&bar_kv[s], 4 * TILE);
-        tma_load_3d(base, &tk, &bar_kv[s], 0, c * C, unit);
-        tma_load_3d(base + TILE, &tk, &bar_kv[s], 64, c * C, unit);
-        tma_load_3d(base + V_OFF, &tv, &bar_kv[s], 0, c * C, unit);
-        tma_load_3d(base + V_OFF + TILE, &tv, &bar_kv[s], 64, c * C, unit);
+        tma_load_3d(base, mk, &bar_kv[s], 0, row, unit);
+        tma_load_3d(base + TILE, mk, &bar_kv[s], 64, row, unit);
+        tma_load_3d(base + V_OFF, mv, &bar_kv[s], 0, row, unit);
+        tma_load_3d(base + V_OFF + TILE, mv, &bar_kv[s], 64, row, unit);
         ++issued[B_KV + s];
     };
     if (tid == 0 && nchunks > 0) {
+        for (int c = -NH; c < 0; ++c) issue_kv(c);
         issue_q(0);
         issue_kv(0);
         if (nchunks > 1) issue_kv(1);
@@ -236,10 +262,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool aborted = false;
     for (int c = 0; c < nchunks; ++c) {
         const int c0 = c * C, n = min(C, L - c0);
-        const uint32_t slot_off = OFF_KV + (c % NR) * KV_SLOT;
+        const uint32_t slot_off = OFF_KV + ((c + NH) % NR) * KV_SLOT;
 
-        // ---- P1: this chunk's tiles, and the previous state update done ----
-        bool ok = wait_bar(B_Q) && wait_bar(B_KV + c % NR);
+        // ---- P1: this chunk's tiles (and the history's), and the previous state update done ----
+        bool ok = true;
+        if (c == 0)
+            for (int hc = 0; hc < NH; ++hc) ok = ok && wait_bar(B_KV + hc);
+        ok = ok && wait_bar(B_Q) && wait_bar(B_KV + (c + NH) % NR);
         if (c > 0) ok = ok && wait_bar(B_ST);
         if (__syncthreads_or(!ok)) { aborted = true; break; }
         tc_fence_after();
@@ -254,8 +283,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
-                if (cj < 0) continue;
-                const uint32_t kb = sb + OFF_KV + (cj % NR) * KV_SLOT;
+                if (cj < -NH) continue;
+                const uint32_t kb = sb + OFF_KV + ((cj + NH) % NR) * KV_SLOT;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t ad = smem_desc(sb + OFF_Q + (kk / 4) * TILE + (kk % 4) * 32, 16, 1024);
@@ -437,7 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int pp = pbase + PART * p + 16 * gq + e;
-                    const bool valid = pp >= 0 && pp <= tg && pp > tg - w;
+                    const bool valid = pp >= -nvalid && pp <= tg && pp > tg - w;
                     x[16 * gq + e] = valid ? __uint_as_float(rr[gq][e]) : -INFINITY;
                     mx = fmaxf(mx, x[16 * gq + e]);
                 }
@@ -507,8 +536,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
-                if (cj < 0) continue;
-                const uint32_t vb = sb + OFF_KV + (cj % NR) * KV_SLOT + V_OFF;
+                if (cj < -NH) continue;
+                const uint32_t vb = sb + OFF_KV + ((cj + NH) % NR) * KV_SLOT + V_OFF;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t ad = smem_desc(vb + kk * 2048, 8192, 1024);
@@ -608,10 +637,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
         for (int e = tid; e < (L - first) * D; e += THREADS) {
             const int tau = first + e / D, i = e % D;
-            rk[(size_t)(tau % w) * D + i] = kp[(size_t)tau * D + i];
-            rv[(size_t)(tau % w) * D + i] = vp[(size_t)tau * D + i];
+            const size_t slot = (size_t)((p0 + tau) % w);  // token p0 + tau
+            rk[slot * D + i] = kp[(size_t)tau * D + i];
+            rv[slot * D + i] = vp[(size_t)tau * D + i];
         }
-        if (h == 0 && tid == 0) a.pos[unit / a.H] = L;
+        if (h == 0 && tid == 0) a.pos[unit / a.H] = p0 + L;
     }
     tc_fence_before();
     __syncthreads();

@@ -107,9 +107,17 @@ struct WsArgs {
     int H, L, w, m;
     // Sequence segments: CTA (unit, seg) covers chunks [seg*seg_chunks,
     // (seg+1)*seg_chunks) and starts from S_init[unit][seg-1] (row = key
-    // dim), the state after the earlier segments; segment 0 starts from 0.
+    // dim), the state after the earlier segments; segment 0 starts from S0.
     const float *S_init;
     int seg_chunks, nseg;
+    // Continuation of a sequence (null / 0 for a prompt from the empty
+    // state): p0[b] is the position of sequence b's first new token, S0
+    // [units][D][D] the start state of segment 0, and HR (64 or 0) the rows
+    // of the window history tile loaded as chunk -1 (tensor maps thk, thv:
+    // row 63 = token p0 - 1, rows past min(p0, w - 1) zero).
+    const int64_t *p0;
+    const float *S0;
+    int HR;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -249,7 +257,8 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int 
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const WsArgs a)
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                      const __grid_constant__ CUtensorMap thk, const __grid_constant__ CUtensorMap thv, const WsArgs a)
 {
     using SM = Smem<NP>;
     using TM = Tmem<NP>;
@@ -283,10 +292,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
     // This CTA's chunks, and the first chunk it loads: the band of its first
-    // chunk reaches NP chunks back into the previous segment.
+    // chunk reaches NP chunks back into the previous segment, or into the
+    // window history (chunk -1) when the prompt continues a sequence.
     const int c_begin = seg * a.seg_chunks, c_end = min(nchunks, c_begin + a.seg_chunks);
-    const int c_lo = c_begin > 0 ? c_begin - NP : 0;
+    const int c_lo = c_begin > 0 || a.HR > 0 ? c_begin - NP : 0;
     const bool last_seg = seg == nseg - 1;
+    // Position of the first token, and the history tokens -nvalid .. -1 in
+    // the window.
+    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
+    const int nvalid = a.HR > 0 ? (int)min(p0, (int64_t)(w - 1)) : 0;
 
     // ---------------------------------------------------------- set-up
     if (warp == W_MMA) {
@@ -315,6 +329,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
         prefetch_tmap(&tg);
+        if (a.HR > 0) {
+            prefetch_tmap(&thk);
+            prefetch_tmap(&thv);
+        }
     }
     // Meta keys of this head into rows 64..79 of every key tile (zero past m).
     for (int e = tid; e < NR * META_ROWS * 64; e += THREADS) {
@@ -342,17 +360,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {}, g_issued = 0;
-            // keys and values of the band chunks before this segment
+            // keys and values of the band chunks before this segment (or of
+            // the window history, chunk -1 = rows 0 .. 63 of the history tile)
             for (int c = c_lo; c < c_begin; ++c) {
                 const int s = (c - c_lo) % NR;
                 uint8_t *base = sm + SM::KV + s * SLOT;
+                const CUtensorMap *mk = c < 0 ? &thk : &tk, *mv = c < 0 ? &thv : &tv;
+                const int row = c < 0 ? a.HR + c * C : c * C;
                 mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
-                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                tma_load_3d(base, mk, &k_full[s], 0, row, unit);
+                tma_load_3d(base + KB_K, mk, &k_full[s], 64, row, unit);
                 ++k_issued[s];
                 mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
-                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                tma_load_3d(base + SLOT_V, mv, &v_full[s], 0, row, unit);
+                tma_load_3d(base + SLOT_V + KB_T, mv, &v_full[s], 64, row, unit);
                 ++v_issued[s];
             }
             for (int c = c_begin; c < c_end && !failed; ++c) {
@@ -501,9 +522,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int j = 32 * quarter + lane;  // value dim = tensor-memory lane
         const uint32_t tl = tmem + tlane(quarter);
         {
-            // Initial state: zero, or the state after the earlier segments.
-            const float *Si = (seg > 0 && a.S_init) ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * D * D + j
-                                                    : nullptr;
+            // Initial state: the state after the earlier segments, or S0
+            // (zero when not given) for the first segment.
+            const float *Si = seg > 0 ? (a.S_init ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * D * D + j
+                                                  : nullptr)
+                                      : (a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr);
 #pragma unroll 1
             for (int cc = 0; cc < D; cc += 16) {
                 uint32_t z[16];
@@ -740,19 +763,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive(&q_empty[qs]);
             }
         }
-        // State hand-off: the last min(L, w) keys and values into the ring, pos = L.
+        // State hand-off: the last min(L, w) keys and values into the ring
+        // (token p0 + tau in slot (p0 + tau) % w), pos = p0 + L.
         if (!failed && a.S_out && last_seg) {
             const int first = max(0, L - w);
             const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
             __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
             for (int e = tp; e < (L - first) * (D / 8); e += PREP_N) {
                 const int tau = first + e / (D / 8), i8 = (e % (D / 8)) * 8;
-                *reinterpret_cast<uint4 *>(rk + (size_t)(tau % w) * D + i8) =
+                const size_t slot = (size_t)((p0 + tau) % w);
+                *reinterpret_cast<uint4 *>(rk + slot * D + i8) =
                     *reinterpret_cast<const uint4 *>(kp + (size_t)tau * D + i8);
-                *reinterpret_cast<uint4 *>(rv + (size_t)(tau % w) * D + i8) =
+                *reinterpret_cast<uint4 *>(rv + slot * D + i8) =
                     *reinterpret_cast<const uint4 *>(vp + (size_t)tau * D + i8);
             }
-            if (h == 0 && tp == 0) a.pos[unit / a.H] = L;
+            if (h == 0 && tp == 0) a.pos[unit / a.H] = p0 + L;
         }
     } else {
         // ------------------------------------------------------ window softmax
@@ -764,10 +789,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int pc = c - c_begin;
             const int c0 = c * C, n = min(C, L - c0);
             const bool rowok = t < n;
-            const int pbase = c0 - 64 * NP;  // global position of band column 0
-            // Keys of row t: positions max(0, tg - w + 1) .. tg, i.e. band
-            // columns lo .. hi.
-            const int hi = t + 64 * NP, lo = max(-pbase, hi - w + 1);
+            const int pbase = c0 - 64 * NP;  // position of band column 0 (the prompt starts at 0)
+            // Keys of row t: positions max(-nvalid, tg - w + 1) .. tg, i.e.
+            // band columns lo .. hi.
+            const int hi = t + 64 * NP, lo = max(-pbase - nvalid, hi - w + 1);
             const int d0 = 16 * hs - lo;
             const uint32_t span = (uint32_t)(hi - lo);
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,

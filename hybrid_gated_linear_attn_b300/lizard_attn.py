@@ -23,8 +23,8 @@ LIZARD_F32, LIZARD_BF16 = 0, 1
 LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
-EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_noalloc", "lizard_attn_decode_step",
-           "lizard_check_device_status", "lizard_status_string")
+EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
+           "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string")
 
 
 class LizardError(RuntimeError):
@@ -59,6 +59,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lizard_state_init.restype = I
         lib.lizard_attn_prefill.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
         lib.lizard_attn_prefill.restype = I
+        lib.lizard_attn_prefill_continue.argtypes = [P, P, P, P, P, F, I, I, P, SP, P]
+        lib.lizard_attn_prefill_continue.restype = I
         lib.lizard_attn_prefill_noalloc.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
         lib.lizard_attn_prefill_noalloc.restype = I
         lib.lizard_attn_decode_step.argtypes = [P, P, P, P, P, F, I, P, SP, P]
@@ -141,6 +143,23 @@ def lizard_attn_prefill(q, k, v, g, meta_k, alpha, w, y=None, state: LizardState
         B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(y),
         ctypes.byref(st) if st is not None else None, _stream(stream))
     _check(rc, "lizard_attn_prefill")
+    return y
+
+
+def lizard_attn_prefill_continue(q, k, v, g, meta_k, alpha, state: LizardState, y=None,
+                                 stream=None) -> torch.Tensor:
+    """L more tokens per sequence ([B,H,L,d] tensors), continuing from
+    ``state`` (updated in place): the window and the gate state carry on
+    from the tokens the state has already consumed."""
+    L = q.shape[2]
+    m = meta_k.shape[1] if meta_k is not None else 0
+    if y is None:
+        y = torch.empty(state.B, state.H, L, state.dv, dtype=q.dtype, device=q.device)
+    st = state.c_struct()
+    rc = library().lizard_attn_prefill_continue(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha), L, m,
+        _ptr(y), ctypes.byref(st), _stream(stream))
+    _check(rc, "lizard_attn_prefill_continue")
     return y
 
 

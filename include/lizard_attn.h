@@ -116,6 +116,38 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
                                   lizard_stream_t stream);
 
 /*
+ * lizard_attn_prefill_continue: L more tokens of each of st->B sequences
+ * and st->H heads, continuing from `st` (read, then updated in place) --
+ * chunked prefill of a long prompt, or a prompt that follows decoded tokens.
+ * The recurrence simply carries on (gist.science/de section 2 item 1: S
+ * holds the whole past of the gate branch; item 2: the anchor window of a
+ * token spans the w most recent tokens, earlier calls' included, which the
+ * ring keeps).  For sequence b with p = pos[b] tokens consumed so far, the
+ * new tokens are positions p .. p + L - 1:
+ *   y_t = q_t S_t + alpha * ya_t,  S_t = diag(sigmoid(g_t)) S_{t-1} + k_t^T v_t
+ * from S_{p-1} = st->S, and the window of position t is positions
+ * max(0, t - w + 1) .. t, those before p read from ring slot (position % w).
+ * Afterwards S is the state after position p + L - 1, ring slot
+ * (position % w) holds the last min(L, w) new keys and values (older slots
+ * are kept), and pos[b] = p + L.  A prefill of L1 tokens followed by a
+ * continuation of L2 gives the y and state of one prefill of L1 + L2 tokens
+ * (up to rounding); the sequences of one call may be at different p.
+ *   q, k, g  [B][H][L][dk]  st->dtype;  v [B][H][L][dv];  meta_k [H][m][dk]
+ *   y        [B][H][L][dv]  st->dtype   output (may not alias an input)
+ * Shapes and paths as lizard_attn_prefill (dk == dv from st).  The call
+ * allocates scratch on `stream` (cudaMallocAsync, freed by cudaFreeAsync on
+ * the same stream) for a copy of pos and of the ring's window history, and
+ * returns LIZARD_ERR_CUDA if that fails.  L == 0 or B == 0 is a no-op.
+ * Precondition: 0 <= pos[b] < 2^40 (a state written by this library always
+ * is); a pos outside that range is reported (lizard_check_device_status)
+ * and read as 0: that sequence's y and state are then undefined, but every
+ * access stays inside the caller's buffers.
+ */
+LIZARD_API lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const void *v, const void *g,
+                                           const void *meta_k, float alpha, int L, int m, void *y,
+                                           const lizard_state *st, lizard_stream_t stream);
+
+/*
  * lizard_attn_prefill_noalloc: lizard_attn_prefill for callers that must not
  * allocate device memory during a call -- for example a serving runtime
  * that reserves all device memory up front for its own pool, code that must
@@ -170,7 +202,8 @@ LIZARD_API lizard_status lizard_attn_decode_step(const void *q, const void *k, c
  * lizard_check_device_status: synchronises `stream`, then reads and clears
  * the library's device error word.  LIZARD_ERR_TIMEOUT if a kernel since the
  * last check abandoned a bounded wait (its outputs are then undefined),
- * LIZARD_ERR_INVALID_ARG if a decode step found a pos outside [0, 2^40), LIZARD_ERR_CUDA if
+ * LIZARD_ERR_INVALID_ARG if a decode step or a continued prefill found a pos
+ * outside [0, 2^40), LIZARD_ERR_CUDA if
  * synchronising failed, LIZARD_OK otherwise.
  */
 LIZARD_API lizard_status lizard_check_device_status(lizard_stream_t stream);

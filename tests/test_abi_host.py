@@ -132,6 +132,30 @@ def test_state_init_rejects(lib):
 
 def test_binding_names_match_the_c_abi():
     import hybrid_gated_linear_attn_b300 as pkg
-    for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_noalloc",
+    for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
                  "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string"):
         assert callable(getattr(pkg, name))
+
+
+def cont(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, L=128, m=4, y=A, st="default"):
+    st = state() if st == "default" else st
+    return lib.lizard_attn_prefill_continue(q, k, v, g, mu, alpha, L, m, y,
+                                            ctypes.byref(st) if st is not None else None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(k=None), INVALID), (dict(g=None), INVALID), (dict(y=None), INVALID),
+    (dict(mu=None), INVALID), (dict(v=MIS), INVALID), (dict(mu=MIS), INVALID),
+    (dict(L=-1), INVALID), (dict(m=-1), INVALID), (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
+    (dict(st=None), INVALID), (dict(st=state(pos=None)), INVALID), (dict(st=state(S=MIS)), INVALID),
+    (dict(st=state(w=0)), INVALID), (dict(st=state(dtype=3)), INVALID),
+    (dict(st=state(dk=96, dv=96)), UNSUPPORTED), (dict(st=state(w=LA.LIZARD_MAX_WINDOW + 1)), UNSUPPORTED),
+])
+def test_continue_rejects(lib, kw, code):
+    assert cont(lib, **kw) == code
+
+
+def test_continue_empty_calls_launch_nothing(lib):
+    # No new token, or no sequence: the state stays as it is and nothing runs.
+    assert cont(lib, q=None, k=None, v=None, g=None, y=None, L=0) == OK
+    assert cont(lib, st=state(Bn=0)) == OK
