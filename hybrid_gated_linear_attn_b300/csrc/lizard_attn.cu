@@ -4,8 +4,8 @@
 // prefill_ws.cuh (bf16, d = 128, w <= 65: warp-specialised tensor cores, with
 // the segment pre-pass of prefill_state.cuh), prefill_tc.cuh (bf16, d = 128,
 // w > 65: tensor cores), prefill_simt.cuh (fp32 and d = 64: CUDA cores, exact
-// fp32), prefill_cont.cuh (inputs of a continued prompt) and the state
-// initialiser below.  Declarations and the contract of every entry point are
+// fp32), prefill_cont.cuh (start position of a continued prompt) and the
+// state initialiser below.  Declarations and the contract of every entry point are
 // in include/lizard_attn.h.
 #include <cuda_runtime.h>
 
@@ -106,51 +106,35 @@ static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps of the window history of a continued prompt ([units][HR][128]
-// bf16); without history they repeat the key and value maps, unread.
-static bool make_history_maps(CUtensorMap *thk, CUtensorMap *thv, const PrefillArgs &pa, const CUtensorMap &tk,
-                              const CUtensorMap &tv)
-{
-    if (pa.HR <= 0) {
-        *thk = tk;
-        *thv = tv;
-        return true;
-    }
-    const int units = pa.B * pa.H;
-    return make_token_map(thk, pa.hist_k, units, pa.HR) && make_token_map(thv, pa.hist_v, units, pa.HR);
-}
-
 static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
 {
     const int units = pa.B * pa.H;
-    CUtensorMap tq, tk, tv, thk, thv;
+    CUtensorMap tq, tk, tv;
     if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
-        !make_token_map(&tv, pa.v, units, pa.L) || !make_history_maps(&thk, &thv, pa, tk, tv))
+        !make_token_map(&tv, pa.v, units, pa.L))
         return LIZARD_ERR_CUDA;
     tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
-                  (pa.w - 1 + tc::C - 1) / tc::C, pa.p0, pa.S0, pa.HR};
-    if (pa.HR != 0 && pa.HR != tc::C * ta.nprev) return LIZARD_ERR_INVALID_ARG;
+                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0};
     auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
                                                                           : tc::prefill_tc_kernel<2>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, thk, thv, ta);
+    kern<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
     return launch_status();
 }
 
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                          const CUtensorMap &tg, const CUtensorMap &thk, const CUtensorMap &thv,
-                                          const ws::WsArgs &wa, int ctas, cudaStream_t s)
+                                          const CUtensorMap &tg, const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
     auto kern = ws::prefill_ws_kernel<NP>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<ctas, ws::THREADS, smem, s>>>(tq, tk, tv, tg, thk, thv, wa);
+    kern<<<ctas, ws::THREADS, smem, s>>>(tq, tk, tv, tg, wa);
     return launch_status();
 }
 
@@ -172,20 +156,24 @@ static int prefill_segments(int units, int nchunks)
 }
 
 // Bytes of scratch a segmented prefill needs: the segment states and decays,
-// and for a continued prompt a copy of its start state.
-static size_t segment_scratch_bytes(int units, int nseg, bool with_start_state = false)
+// and for a continued prompt copies of its start state and window history.
+static size_t segment_states_bytes(int units, int nseg)
 {
-    return (size_t)units * (nseg - 1) * ((size_t)ws::D * ws::D + ws::D) * sizeof(float) +
-           (with_start_state ? (size_t)units * ws::D * ws::D * sizeof(float) : 0);
+    return (size_t)units * (nseg - 1) * ((size_t)ws::D * ws::D + ws::D) * sizeof(float);
+}
+static size_t segment_scratch_bytes(int units, int nseg, bool cont = false)
+{
+    return segment_states_bytes(units, nseg) +
+           (cont ? (size_t)units * (ws::D * ws::D * sizeof(float) + 2 * ws::C * ws::D * sizeof(__nv_bfloat16)) : 0);
 }
 
 // The segment pre-pass: end state and total decay of every segment but the
 // last, then the start state of every segment (written over the end states).
-// S0 (nullable) is the start state of the prompt; S0_copy receives a copy of
-// it for the first segment.
+// For a continued prompt `sc` names its start state and the copies the
+// first segment reads.
 static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tg,
                                            float *scratch, int units, int L, int seg_chunks, int nseg,
-                                           const float *S0, float *S0_copy, cudaStream_t s)
+                                           const seg::ScanCont &sc, cudaStream_t s)
 {
     seg::SegArgs sa{scratch, scratch + (size_t)units * (nseg - 1) * ws::D * ws::D, L, seg_chunks, nseg};
     if (cudaFuncSetAttribute(seg::segment_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -193,8 +181,7 @@ static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensor
         return LIZARD_ERR_CUDA;
     seg::segment_state_kernel<<<units * (nseg - 1), seg::THREADS, seg::SMEM_BYTES, s>>>(tk, tv, tg, sa);
     if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
-    seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, units, nseg, S0,
-                                                                            S0_copy);
+    seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, units, nseg, sc);
     return launch_status();
 }
 
@@ -213,16 +200,14 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
     const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
     nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
     if (nseg < 1) nseg = 1;
-    if (pa.HR != 0 && pa.HR != (pa.w > 1 ? ws::C : 0)) return LIZARD_ERR_INVALID_ARG;
-    CUtensorMap tq, tk, tv, tg, thk, thv;
+    CUtensorMap tq, tk, tv, tg;
     if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
-        !make_token_map(&tv, pa.v, units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L) ||
-        !make_history_maps(&thk, &thv, pa, tk, tv))
+        !make_token_map(&tv, pa.v, units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
         return LIZARD_ERR_CUDA;
     float *seg_states = nullptr;
     bool owned = false;
     if (nseg > 1) {
-        const size_t need = segment_scratch_bytes(units, nseg, pa.S0 != nullptr);
+        const size_t need = segment_scratch_bytes(units, nseg, pa.cont != 0);
         if (scratch) {
             if (scratch_bytes < need) return LIZARD_ERR_UNSUPPORTED;
             seg_states = scratch;
@@ -234,24 +219,33 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
         }
     }
     lizard_status rc = LIZARD_OK;
-    // Start state of the first segment: S0 itself when one CTA walks the
-    // whole prompt (it reads S0 before it writes the final state over it),
-    // else a copy that the scan makes.
+    // Start state and window history of the first segment: read in place
+    // when one CTA walks the whole prompt (it reads them before it writes the
+    // state), else copies that the scan makes.
     const float *seg0_state = pa.S0;
+    const __nv_bfloat16 *hist = nullptr;
     if (nseg > 1) {
-        float *copy = pa.S0 ? seg_states + (size_t)units * (nseg - 1) * (ws::D * ws::D + ws::D) : nullptr;
-        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, pa.S0, copy, s);
-        seg0_state = copy;
+        seg::ScanCont sc{};
+        if (pa.cont) {
+            float *copy = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(seg_states) +
+                                                    segment_states_bytes(units, nseg));
+            __nv_bfloat16 *hcopy = reinterpret_cast<__nv_bfloat16 *>(copy + (size_t)units * ws::D * ws::D);
+            sc = seg::ScanCont{pa.S0, copy, static_cast<const __nv_bfloat16 *>(pa.ring_k),
+                               static_cast<const __nv_bfloat16 *>(pa.ring_v), pa.pos, hcopy, pa.H, pa.w};
+            seg0_state = copy;
+            hist = hcopy;
+        }
+        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, sc, s);
     }
     ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
                   nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg,
-                  pa.p0, seg0_state, pa.HR};
+                  pa.cont, seg0_state, hist};
     if (rc == LIZARD_OK)
-        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, thk, thv, wa, units * nseg, s)
-                       : launch_prefill_ws_np<1>(tq, tk, tv, tg, thk, thv, wa, units * nseg, s);
+        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units * nseg, s)
+                       : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units * nseg, s);
     if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -421,36 +415,16 @@ lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const v
     if (m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
     const int B = st->B, H = st->H, dk = st->dk, w = st->w;
     if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
+    // The CTAs of one sequence count their arrivals in pos's high bits
+    // (H x segments of at most the SM count must stay below 2^23).
+    if (H > 16384) return LIZARD_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return LIZARD_OK;  // no new token: the state stays as it is
-    const int units = B * H;
-    // Window history rows: the previous ceil((w - 1) / 64) chunks.
-    const int HR = 64 * ((w - 1 + 63) / 64);
-    const size_t row_bytes = (size_t)dk * esize(st->dtype);
-    const size_t p0_bytes = ((size_t)B * sizeof(int64_t) + 255) & ~(size_t)255;
-    const size_t hist_bytes = (size_t)units * HR * row_bytes;
+    PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m, st->S, st->ring_k, st->ring_v, st->pos, 1, st->S};
     cudaStream_t s = (cudaStream_t)stream;
-    uint8_t *scratch = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), p0_bytes + 2 * hist_bytes, s) != cudaSuccess) {
-        cudaGetLastError();
-        return LIZARD_ERR_CUDA;
-    }
-    int64_t *p0 = reinterpret_cast<int64_t *>(scratch);
-    uint8_t *hist_k = scratch + p0_bytes, *hist_v = hist_k + hist_bytes;
-    continue_prologue_kernel<<<units, CONT_THREADS, 0, s>>>(
-        static_cast<const uint4 *>(st->ring_k), static_cast<const uint4 *>(st->ring_v), st->pos, H, w, HR,
-        (int)(row_bytes / 16), reinterpret_cast<uint4 *>(hist_k), reinterpret_cast<uint4 *>(hist_v), p0);
-    rc = launch_status();
-    if (rc == LIZARD_OK) {
-        PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m, st->S, st->ring_k, st->ring_v, st->pos,
-                       p0, hist_k, hist_v, HR, st->S};
-        if (st->dtype == LIZARD_BF16)
-            rc = dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
-                           : launch_prefill<__nv_bfloat16, 64>(pa, s);
-        else
-            rc = dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
-    }
-    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
-    return rc;
+    if (st->dtype == LIZARD_BF16)
+        return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
+                         : launch_prefill<__nv_bfloat16, 64>(pa, s);
+    return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 
 lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,

@@ -18,6 +18,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "prefill_cont.cuh"
 
 namespace lizard {
 
@@ -30,13 +31,12 @@ struct PrefillArgs {
     float *S_out;
     void *ring_k, *ring_v;
     int64_t *pos;
-    // Continuation of a sequence (all null / 0 for a prompt from the empty
-    // state): p0[b] is the position of sequence b's first new token, hist_k /
-    // hist_v [units][HR][d] the tokens before it (row HR - 1 = token p0 - 1;
-    // rows past min(p0, w - 1) are zero) and S0 [units][d][d] the start state.
-    const int64_t *p0;
-    const void *hist_k, *hist_v;
-    int HR;
+    // Continuation of a sequence (0 / null for a prompt from the empty
+    // state): with cont = 1 every CTA takes the start position from pos
+    // (take_start_position) and reads the window history from the ring; S0
+    // [units][d][d] is the start state (may be S_out: each CTA reads its own
+    // unit's S0 before it writes S_out).
+    int cont;
     const float *S0;
 };
 
@@ -79,14 +79,18 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
     const T *g = static_cast<const T *>(a.g) + base;
     const T *mu = static_cast<const T *>(a.mu) + (size_t)h * m * D;
     T *y = static_cast<T *>(a.y) + base;
-    const T *hk = a.HR ? static_cast<const T *>(a.hist_k) + (size_t)unit * a.HR * D : nullptr;
-    const T *hv = a.HR ? static_cast<const T *>(a.hist_v) + (size_t)unit * a.HR * D : nullptr;
-    // Window keys before the prompt: tokens -nvalid .. -1 (hist row HR + tau).
-    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
-    const int nvalid = a.HR ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    // Start position p0 (0 for a prompt from the empty state) and the
+    // window keys before the prompt: tokens -nvalid .. -1, ring slot (p0 + tau) % w.
+    __shared__ int64_t p0_sh;
+    if (tid == 0) p0_sh = a.cont ? take_start_position(a.pos + unit / a.H, a.H, L) : 0;
+    const T *ring_k = a.cont ? static_cast<const T *>(a.ring_k) + (size_t)unit * w * D : nullptr;
+    const T *ring_v = a.cont ? static_cast<const T *>(a.ring_v) + (size_t)unit * w * D : nullptr;
 
     const float *S0 = a.S0 ? a.S0 + (size_t)unit * D * D : nullptr;
     for (int i = tid; i < D * D; i += SIMT_THREADS) S_s[i] = S0 ? S0[i] : 0.f;
+    __syncthreads();
+    const int64_t p0 = p0_sh;
+    const int nvalid = a.cont ? (int)min(p0, (int64_t)(w - 1)) : 0;
 
     for (int c0 = 0; c0 < L; c0 += C) {
         const int n = min(C, L - c0);
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
                     if (tau >= c0) {
                         for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * k_s[(tau - c0) * LD + i];
                     } else {
-                        const T *kr = tau >= 0 ? k + (size_t)tau * D : hk + (size_t)(a.HR + tau) * D;
+                        const T *kr = tau >= 0 ? k + (size_t)tau * D : history_row(ring_k, p0, tau, nvalid, w, D);
                         for (int i = lane; i < D; i += 32) part += q_s[t * LD + i] * to_f32(kr[i]);
                     }
                 } else {
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
                     const int j = lane + 32 * jj;
                     const float vv = tau >= c0 ? v_s[(tau - c0) * D + j]
                                      : tau >= 0 ? to_f32(v[(size_t)tau * D + j])
-                                                : to_f32(hv[(size_t)(a.HR + tau) * D + j]);
+                                                : to_f32(history_row(ring_v, p0, tau, nvalid, w, D)[j]);
                     acc[jj] += pc * vv;
                 }
             }
@@ -210,7 +214,8 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
     }
     __syncthreads();
     // 6. State out: S, the last min(L, w) tokens into the ring (token p0 + tau
-    //    in slot (p0 + tau) % w), pos = p0 + L.
+    //    in slot (p0 + tau) % w), pos = L (a continued prompt advanced pos
+    //    when it started).
     if (a.S_out) {
         float *So = a.S_out + (size_t)unit * D * D;
         for (int i = tid; i < D * D; i += SIMT_THREADS) So[i] = S_s[i];
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
             rk[slot * D + i] = k[(size_t)tau * D + i];
             rv[slot * D + i] = v[(size_t)tau * D + i];
         }
-        if (h == 0 && tid == 0) a.pos[unit / a.H] = p0 + L;
+        if (!a.cont && h == 0 && tid == 0) a.pos[unit / a.H] = L;
     }
 }
 

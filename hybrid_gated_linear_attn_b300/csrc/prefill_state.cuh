@@ -240,22 +240,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == W_MMA) tmem_dealloc(tmem, 128);
 }
 
+// A continued prompt (Lizard, gist.science/de section 2 items 1-2: the
+// state and the anchor window carry on from earlier tokens): its start
+// state S0 and the state's pos and ring, from which the scan copies what the
+// first segment reads -- the last segment writes S and the ring in place.
+// All null for a prompt from the empty state.
+struct ScanCont {
+    const float *S0;
+    float *S0_copy;                          // [units][D][D]
+    const __nv_bfloat16 *ring_k, *ring_v;    // [units][w][D]
+    const int64_t *pos;                      // [B]
+    __nv_bfloat16 *hist;                     // [units][2][C][D]: keys, values of tokens -C .. -1
+    int H, w;
+};
+
 // Segment start states: S_start(0) = S0 (zero when S0 is null) and
 // S_start(p+1) = diag(2^{Lam_p}) S_start(p) + dS_p, written over dS_p, so
-// that dS[u][p] holds S_start(p + 1) afterwards.  S0_copy (nullable)
-// receives a copy of S0 for the first segment, which must not read S0 in
-// place: the last segment writes the final state over it.  One thread per
-// state element and unit.
-__global__ void segment_scan_kernel(float *dS, const float *lam, int units, int nseg, const float *S0,
-                                    float *S0_copy)
+// that dS[u][p] holds S_start(p + 1) afterwards.  For a continued prompt
+// the first segment's inputs are copied as well: S0, and the window history
+// (row r = token r - C, from ring slot (p0 + r - C) % w with p0 = the low 40
+// bits of pos, as the prefill takes it; zero rows where no key).  One
+// thread per state element and unit.
+__global__ void segment_scan_kernel(float *dS, const float *lam, int units, int nseg, ScanCont sc)
 {
     const int nsp = nseg - 1;
     const int u = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;  // i * D + j
     if (u >= units || e >= D * D) return;
+    if (sc.hist && e < 2 * C * (D / 8)) {
+        const int kv = e / (C * (D / 8)), r = (e / (D / 8)) % C, i8 = (e % (D / 8)) * 8;
+        const int64_t p0 = (int64_t)((unsigned long long)sc.pos[u / sc.H] & (CONT_POS_TICK - 1));
+        const int nvalid = (int)min(p0, (int64_t)(sc.w - 1));
+        const __nv_bfloat16 *ring = (kv ? sc.ring_v : sc.ring_k) + (size_t)u * sc.w * D;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r - C >= -nvalid)
+            val = *reinterpret_cast<const uint4 *>(ring + (size_t)((p0 + r - C) % sc.w) * D + i8);
+        *reinterpret_cast<uint4 *>(sc.hist + (((size_t)u * 2 + kv) * C + r) * D + i8) = val;
+    }
     const int i = e / D;
-    float S = S0 ? S0[(size_t)u * D * D + e] : 0.f;
-    if (S0_copy) S0_copy[(size_t)u * D * D + e] = S;
+    float S = sc.S0 ? sc.S0[(size_t)u * D * D + e] : 0.f;
+    if (sc.S0_copy) sc.S0_copy[(size_t)u * D * D + e] = S;
     for (int q = 0; q < nsp; ++q) {
         const size_t off = ((size_t)u * nsp + q) * D * D + e;
         S = exp2f(lam[((size_t)u * nsp + q) * D + i]) * S + dS[off];

@@ -37,6 +37,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "prefill_cont.cuh"
 #include "sm100.cuh"
 
 namespace lizard {
@@ -87,14 +88,13 @@ struct TcArgs {
     int64_t *pos;
     float alpha;
     int H, L, w, m, nprev;
-    // Continuation of a sequence (null / 0 for a prompt from the empty
-    // state): p0[b] is the position of sequence b's first new token, S0
-    // [units][D][D] the start state, and HR (64 * nprev or 0) the rows of the
-    // window history loaded as chunks -nprev .. -1 (tensor maps thk, thv:
-    // row HR - 1 = token p0 - 1, rows past min(p0, w - 1) zero).
-    const int64_t *p0;
+    // Continuation of a sequence (0 / null for a prompt from the empty
+    // state): with cont = 1 the CTA takes the start position from pos
+    // (take_start_position) and reads the window history, chunks -nprev ..
+    // -1, from the ring; S0 [units][D][D] is the start state (may be S_out:
+    // the CTA reads it before it writes S_out).
+    int cont;
     const float *S0;
-    int HR;
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -134,8 +134,7 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi)
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap thk,
-                      const __grid_constant__ CUtensorMap thv, const TcArgs a)
+                      const __grid_constant__ CUtensorMap tv, const TcArgs a)
 {
     constexpr int NB = NP + 1;     // band chunks
     constexpr int PART = 16 * NB;  // band columns per softmax thread (four threads per row)
@@ -148,18 +147,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *bar_q = bars, *bar_kv = bars + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
+    int64_t *p0_slot = reinterpret_cast<int64_t *>(bars + NBARS + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int unit = blockIdx.x, h = unit % a.H;
     const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
-    // Window history: NH chunks before the prompt (chunks -NH .. -1), of
-    // which tokens -nvalid .. -1 are keys.  Chunk c lives in k/v slot
-    // (c + NH) % NR.
-    const int NH = a.HR > 0 ? NP : 0;
-    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
-    const int nvalid = NH > 0 ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    // Window history of a continued prompt: NH chunks before the prompt
+    // (chunks -NH .. -1), of which tokens -nvalid .. -1 are keys.  Chunk c
+    // lives in k/v slot (c + NH) % NR.
+    const int NH = a.cont ? NP : 0;
     // Prep mapping: key dims 2ip and 2ip+1, tokens 16*tqr .. 16*tqr+15.
     const int ip = tid & 63, tqr = tid >> 6;
     // Softmax mapping (M = 64 accumulator layout): row srow, column part 2*half + ssub.
@@ -175,10 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
-        if (NH > 0) {
-            prefetch_tmap(&thk);
-            prefetch_tmap(&thv);
-        }
+        *p0_slot = a.cont ? take_start_position(a.pos + unit / a.H, a.H, L) : 0;
     }
     // Meta keys of this head, zero rows past m.
     for (int e = tid; e < META_ROWS * D; e += THREADS) {
@@ -190,6 +185,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int64_t p0 = *p0_slot;
+    const int nvalid = NH > 0 ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    if (NH > 0) {
+        // History chunks into slots 0 .. NH-1 (zero rows where no key), in the
+        // swizzled layout of a TMA-loaded tile; read from the ring, which this
+        // CTA writes only at its end.
+        const __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = tid; e < NH * C * (D / 8); e += THREADS) {
+            const int hc = e / (C * (D / 8)), rem = e % (C * (D / 8)), r = rem / (D / 8), i8 = (rem % (D / 8)) * 8;
+            const int tau = (hc - NH) * C + r;
+            const __nv_bfloat16 *kr = history_row(rk, p0, tau, nvalid, w, D);
+            const __nv_bfloat16 *vr = history_row(rv, p0, tau, nvalid, w, D);
+            const uint32_t off = hc * KV_SLOT + (i8 / 64) * TILE + sw128_offset(r, (i8 % 64) * 2);
+            *reinterpret_cast<uint4 *>(sm + OFF_KV + off) = kr ? *reinterpret_cast<const uint4 *>(kr + i8) : zero;
+            *reinterpret_cast<uint4 *>(sm + OFF_KV + V_OFF + off) =
+                vr ? *reinterpret_cast<const uint4 *>(vr + i8) : zero;
+        }
+        fence_proxy_async_smem();
+    }
     if (warp < 4) {  // S^T = S0^T (zero when not given)
         const int j = 32 * quarter + lane;
         const float *Si = a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr;
@@ -224,20 +239,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sm + OFF_Q + TILE, &tq, bar_q, 64, c * C, unit);
         ++issued[B_Q];
     };
-    auto issue_kv = [&](int c) {  // c < 0: a chunk of the window history
+    auto issue_kv = [&](int c) {
         const int s = (c + NH) % NR;
         uint8_t *base = sm + OFF_KV + s * KV_SLOT;
-        const CUtensorMap *mk = c < 0 ? &thk : &tk, *mv = c < 0 ? &thv : &tv;
-        const int row = c < 0 ? a.HR + c * C : c * C;
         mbar_arrive_expect_tx(&bar_kv[s], 4 * TILE);
-        tma_load_3d(base, mk, &bar_kv[s], 0, row, unit);
-        tma_load_3d(base + TILE, mk, &bar_kv[s], 64, row, unit);
-        tma_load_3d(base + V_OFF, mv, &bar_kv[s], 0, row, unit);
-        tma_load_3d(base + V_OFF + TILE, mv, &bar_kv[s], 64, row, unit);
+        tma_load_3d(base, &tk, &bar_kv[s], 0, c * C, unit);
+        tma_load_3d(base + TILE, &tk, &bar_kv[s], 64, c * C, unit);
+        tma_load_3d(base + V_OFF, &tv, &bar_kv[s], 0, c * C, unit);
+        tma_load_3d(base + V_OFF + TILE, &tv, &bar_kv[s], 64, c * C, unit);
         ++issued[B_KV + s];
     };
     if (tid == 0 && nchunks > 0) {
-        for (int c = -NH; c < 0; ++c) issue_kv(c);
         issue_q(0);
         issue_kv(0);
         if (nchunks > 1) issue_kv(1);
@@ -264,11 +276,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int c0 = c * C, n = min(C, L - c0);
         const uint32_t slot_off = OFF_KV + ((c + NH) % NR) * KV_SLOT;
 
-        // ---- P1: this chunk's tiles (and the history's), and the previous state update done ----
-        bool ok = true;
-        if (c == 0)
-            for (int hc = 0; hc < NH; ++hc) ok = ok && wait_bar(B_KV + hc);
-        ok = ok && wait_bar(B_Q) && wait_bar(B_KV + (c + NH) % NR);
+        // ---- P1: this chunk's tiles, and the previous state update done ----
+        bool ok = wait_bar(B_Q) && wait_bar(B_KV + (c + NH) % NR);
         if (c > 0) ok = ok && wait_bar(B_ST);
         if (__syncthreads_or(!ok)) { aborted = true; break; }
         tc_fence_after();
@@ -641,7 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             rk[slot * D + i] = kp[(size_t)tau * D + i];
             rv[slot * D + i] = vp[(size_t)tau * D + i];
         }
-        if (h == 0 && tid == 0) a.pos[unit / a.H] = p0 + L;
+        if (!a.cont && h == 0 && tid == 0) a.pos[unit / a.H] = L;  // (a continued prompt advanced pos at its start)
     }
     tc_fence_before();
     __syncthreads();

@@ -41,6 +41,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "prefill_cont.cuh"
 #include "sm100.cuh"
 
 namespace lizard {
@@ -110,14 +111,17 @@ struct WsArgs {
     // dim), the state after the earlier segments; segment 0 starts from S0.
     const float *S_init;
     int seg_chunks, nseg;
-    // Continuation of a sequence (null / 0 for a prompt from the empty
-    // state): p0[b] is the position of sequence b's first new token, S0
-    // [units][D][D] the start state of segment 0, and HR (64 or 0) the rows
-    // of the window history tile loaded as chunk -1 (tensor maps thk, thv:
-    // row 63 = token p0 - 1, rows past min(p0, w - 1) zero).
-    const int64_t *p0;
+    // Continuation of a sequence (0 / null for a prompt from the empty
+    // state): with cont = 1 every CTA takes the start position from pos
+    // (take_start_position) and the first segment sees the window history
+    // as chunk -1: from `hist` ([units][2][64][D], keys then values, row r =
+    // token r - 64, zero where no key) when given, else from the ring, which
+    // the CTA then writes only at its end (one segment).  S0 [units][D][D] is
+    // the start state of the first segment (may be S_out when there is one
+    // segment: it is read before S_out is written).
+    int cont;
     const float *S0;
-    int HR;
+    const __nv_bfloat16 *hist;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -257,8 +261,7 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int 
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-                      const __grid_constant__ CUtensorMap thk, const __grid_constant__ CUtensorMap thv, const WsArgs a)
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const WsArgs a)
 {
     using SM = Smem<NP>;
     using TM = Tmem<NP>;
@@ -295,12 +298,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // chunk reaches NP chunks back into the previous segment, or into the
     // window history (chunk -1) when the prompt continues a sequence.
     const int c_begin = seg * a.seg_chunks, c_end = min(nchunks, c_begin + a.seg_chunks);
-    const int c_lo = c_begin > 0 || a.HR > 0 ? c_begin - NP : 0;
+    const int c_lo = c_begin > 0 || a.cont ? c_begin - NP : 0;
     const bool last_seg = seg == nseg - 1;
-    // Position of the first token, and the history tokens -nvalid .. -1 in
-    // the window.
-    const int64_t p0 = a.p0 ? a.p0[unit / a.H] : 0;
-    const int nvalid = a.HR > 0 ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    int64_t *p0_slot = reinterpret_cast<int64_t *>(sm + SM::TSLOT + 8);
 
     // ---------------------------------------------------------- set-up
     if (warp == W_MMA) {
@@ -329,9 +329,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
         prefetch_tmap(&tg);
-        if (a.HR > 0) {
-            prefetch_tmap(&thk);
-            prefetch_tmap(&thv);
+        *p0_slot = a.cont ? take_start_position(a.pos + unit / a.H, a.H * nseg, L) : 0;
+    }
+    if (a.cont) __syncthreads();  // p0
+    // Start position (0 for a prompt from the empty state; read from shared
+    // memory only after the barrier above), and the history tokens
+    // -nvalid .. -1 in the window.
+    const int64_t p0 = a.cont ? *p0_slot : 0;
+    const int nvalid = a.cont ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    if (c_lo < 0) {
+        // Window history (chunk -1) into k/v slot 0, zero rows where no key,
+        // in the swizzled layout of a TMA-loaded tile.
+        const __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
+        const __nv_bfloat16 *hk = a.hist ? a.hist + (size_t)unit * 2 * C * D : nullptr;
+        const __nv_bfloat16 *hv = a.hist ? hk + C * D : nullptr;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = tid; e < C * (D / 8); e += THREADS) {
+            const int r = e / (D / 8), i8 = (e % (D / 8)) * 8;
+            const __nv_bfloat16 *kr = hk ? hk + (size_t)r * D : history_row(rk, p0, r - C, nvalid, w, D);
+            const __nv_bfloat16 *vr = hk ? hv + (size_t)r * D : history_row(rv, p0, r - C, nvalid, w, D);
+            const uint32_t sw = sw128_offset(r, (i8 % 64) * 2);
+            *reinterpret_cast<uint4 *>(sm + SM::KV + (i8 / 64) * KB_K + sw) =
+                kr ? *reinterpret_cast<const uint4 *>(kr + i8) : zero;
+            *reinterpret_cast<uint4 *>(sm + SM::KV + SLOT_V + (i8 / 64) * KB_T + sw) =
+                vr ? *reinterpret_cast<const uint4 *>(vr + i8) : zero;
         }
     }
     // Meta keys of this head into rows 64..79 of every key tile (zero past m).
@@ -360,20 +381,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {}, g_issued = 0;
-            // keys and values of the band chunks before this segment (or of
-            // the window history, chunk -1 = rows 0 .. 63 of the history tile)
+            // keys and values of the band chunks before this segment; the
+            // window history (chunk -1) is in place since the set-up
             for (int c = c_lo; c < c_begin; ++c) {
                 const int s = (c - c_lo) % NR;
                 uint8_t *base = sm + SM::KV + s * SLOT;
-                const CUtensorMap *mk = c < 0 ? &thk : &tk, *mv = c < 0 ? &thv : &tv;
-                const int row = c < 0 ? a.HR + c * C : c * C;
-                mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                tma_load_3d(base, mk, &k_full[s], 0, row, unit);
-                tma_load_3d(base + KB_K, mk, &k_full[s], 64, row, unit);
+                if (c < 0) {
+                    mbar_arrive(&k_full[s]);
+                    mbar_arrive(&v_full[s]);
+                } else {
+                    mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
+                    tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
+                    tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                    mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
+                    tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
+                    tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                }
                 ++k_issued[s];
-                mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                tma_load_3d(base + SLOT_V, mv, &v_full[s], 0, row, unit);
-                tma_load_3d(base + SLOT_V + KB_T, mv, &v_full[s], 64, row, unit);
                 ++v_issued[s];
             }
             for (int c = c_begin; c < c_end && !failed; ++c) {
@@ -764,7 +788,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // State hand-off: the last min(L, w) keys and values into the ring
-        // (token p0 + tau in slot (p0 + tau) % w), pos = p0 + L.
+        // (token p0 + tau in slot (p0 + tau) % w), pos = L (a continued
+        // prompt advanced pos at its start).
         if (!failed && a.S_out && last_seg) {
             const int first = max(0, L - w);
             const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
@@ -777,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *reinterpret_cast<uint4 *>(rv + slot * D + i8) =
                     *reinterpret_cast<const uint4 *>(vp + (size_t)tau * D + i8);
             }
-            if (h == 0 && tp == 0) a.pos[unit / a.H] = p0 + L;
+            if (!a.cont && h == 0 && tp == 0) a.pos[unit / a.H] = L;
         }
     } else {
         // ------------------------------------------------------ window softmax

@@ -134,14 +134,17 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
  * (up to rounding); the sequences of one call may be at different p.
  *   q, k, g  [B][H][L][dk]  st->dtype;  v [B][H][L][dv];  meta_k [H][m][dk]
  *   y        [B][H][L][dv]  st->dtype   output (may not alias an input)
- * Shapes and paths as lizard_attn_prefill (dk == dv from st).  The call
- * allocates scratch on `stream` (cudaMallocAsync, freed by cudaFreeAsync on
- * the same stream) for a copy of pos and of the ring's window history, and
- * returns LIZARD_ERR_CUDA if that fails.  L == 0 or B == 0 is a no-op.
- * Precondition: 0 <= pos[b] < 2^40 (a state written by this library always
- * is); a pos outside that range is reported (lizard_check_device_status)
- * and read as 0: that sequence's y and state are then undefined, but every
- * access stays inside the caller's buffers.
+ * Shapes and paths as lizard_attn_prefill (dk == dv from st; H <= 16384).
+ * Like lizard_attn_prefill it allocates only when a prompt runs as sequence
+ * segments (few batch x head units, long L): then the segments' start
+ * states and a copy of the first segment's S and window history live in
+ * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * L == 0 or B == 0 is a no-op.  Precondition: 0 <= pos[b] < 2^40 (a state
+ * written by this library always is).  While the call runs, pos[b] carries
+ * an arrival count in its high bits; it holds p + L again once the work is
+ * done.  A pos outside that range is reported (lizard_check_device_status);
+ * that sequence's y, S, ring and pos are then undefined, but every access
+ * stays inside the caller's buffers.
  */
 LIZARD_API lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const void *v, const void *g,
                                            const void *meta_k, float alpha, int L, int m, void *y,
