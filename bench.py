@@ -41,7 +41,7 @@ METRIC = "prefill tokens/s & % bf16 TC roofline; decode tokens/s & HBM GB/s (1 B
 PREFILL_WL = WORKLOADS["llama3_8b"]
 DECODE_WL = WORKLOADS["decode"]
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-PREFILL_KERNEL_SRC = ["csrc/prefill_ws.cuh", "csrc/sm100.cuh", "csrc/common.cuh"]
+PREFILL_KERNEL_SRC = ["csrc/prefill_ws.cuh", "csrc/prefill_cont.cuh", "csrc/sm100.cuh", "csrc/common.cuh"]
 DECODE_KERNEL_SRC = ["csrc/decode.cuh", "csrc/common.cuh"]
 
 
