@@ -387,3 +387,238 @@ int oracle_gla_product_form(int dtype, const void *q, const void *k, const void 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass (reverse mode of the forward above).                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gradients of a scalar loss with respect to every input of the operator,
+ * given dy = dLoss/dy, for sequences that start from the empty state (no S0,
+ * no window history): the training case.  Lizard (gist.science/de section 2)
+ * trains the gate (item 1), the meta-memory keys (item 2) and alpha (item 3)
+ * along with the inputs; the gradients follow from the forward definitions
+ * by the chain rule, step by step in reverse:
+ *
+ *   Combine   y_t = yg_t + alpha ya_t:
+ *             dyg_t = dy_t,  dya_t = alpha dy_t,  dalpha += dy_t . ya_t
+ *   Gate      yg_t = q_t S_t,  S_t = diag(gamma_t) S_{t-1} + k_t^T v_t,
+ *             walked from t = L-1 down to 0 with G = dLoss/dS_t:
+ *               G      += q_t^T dyg_t
+ *               dq_t   += dyg_t S_t^T  (dq_t[i] = sum_j dyg_t[j] S_t[i][j])
+ *               dk_t   += G v_t^T  (dk_t[i] = sum_j G[i][j] v_t[j])
+ *               dv_t   += k_t G    (dv_t[j] = sum_i k_t[i] G[i][j])
+ *               dgamma_t[i] = sum_j G[i][j] S_{t-1}[i][j]
+ *               G       = diag(gamma_t) G          (now dLoss/dS_{t-1})
+ *             dg_t = dgamma_t * sigmoid(g_t) * sigmoid(-g_t).
+ *   Anchor    p_s = e^{a_s - M} / Z over the window keys s and the sinks j
+ *             (value 0), ya_t = sum_s p_s v_s:
+ *               dv_s += p_s dya_t;   dp_s = dya_t . v_s  (sinks: dp_j = 0)
+ *               da_s  = p_s (dp_s - sum_s' p_s' dp_s'),  dc_j = p_j (0 - same sum)
+ *               dq_t += sum_s da_s k_s + sum_j dc_j mu_j
+ *               dk_s += da_s q_t;    dmu_j += dc_j q_t
+ *
+ * The states S_t are those of the forward loop: the walk keeps S at every
+ * CKPT-th token and re-runs the identical update to rebuild the states of
+ * one block before walking it backwards (memory O((L/CKPT + CKPT) dk dv)
+ * instead of O(L dk dv); every value is the forward's, bit for bit).
+ */
+#define CKPT 64
+
+typedef struct {
+    int dtype;
+    const void *q, *k, *v, *g, *mu;
+    double alpha;
+    int H, L, dk, dv, w, m;
+    const double *dy;          /* [U][L][dv] */
+    double *dq, *dk_, *dv_, *dg; /* [U][L][dk] (dv_: [U][L][dv]) */
+    double *dmu;               /* [U][m][dk] per unit */
+    double *dalpha;            /* [U] per unit */
+    int unit0, u_begin, u_end;
+} bwd_args;
+
+/* S <- diag(gamma_t) S + k_t^T v_t for token t of one unit (as in forward_unit). */
+static void gate_step(const bwd_args *a, size_t qo, size_t vo, int t, double *S)
+{
+    const int dk = a->dk, dv = a->dv;
+    for (int i = 0; i < dk; ++i) {
+        double gam = exp(oracle_log_sigmoid(ld(a->dtype, a->g, qo + (size_t)t * dk + i)));
+        double ki = ld(a->dtype, a->k, qo + (size_t)t * dk + i);
+        for (int j = 0; j < dv; ++j)
+            S[(size_t)i * dv + j] = gam * S[(size_t)i * dv + j] + ki * ld(a->dtype, a->v, vo + (size_t)t * dv + j);
+    }
+}
+
+static void backward_unit(const bwd_args *a, int u)
+{
+    const int L = a->L, dk = a->dk, dv = a->dv, w = a->w, m = a->m;
+    const int h = (a->unit0 + u) % a->H;
+    const size_t qo = (size_t)u * L * dk, vo = (size_t)u * L * dv;
+    const size_t SS = (size_t)dk * dv;
+    const int nck = (L + CKPT - 1) / CKPT;
+    double *ck = calloc((size_t)(nck > 0 ? nck : 1) * SS, sizeof *ck);  /* S before block c */
+    double *blk = malloc(sizeof(double) * (CKPT + 1) * SS);             /* S_{t0-1} .. S_{t0+CKPT-1} */
+    double *G = calloc(SS, sizeof *G);
+    double *qt = malloc(sizeof(double) * dk), *dyt = malloc(sizeof(double) * dv);
+    double *ya = malloc(sizeof(double) * dv), *sc = malloc(sizeof(double) * ((size_t)w + m));
+    double *dmu = a->dmu + (size_t)u * m * dk;
+    double dalpha = 0;
+
+    for (size_t e = 0; e < (size_t)L * dk; ++e) { a->dq[qo + e] = 0; a->dk_[qo + e] = 0; a->dg[qo + e] = 0; }
+    for (size_t e = 0; e < (size_t)L * dv; ++e) a->dv_[vo + e] = 0;
+    for (size_t e = 0; e < (size_t)m * dk; ++e) dmu[e] = 0;
+
+    /* Checkpoints: the state before every block of CKPT tokens. */
+    {
+        double *S = calloc(SS, sizeof *S);
+        for (int t = 0; t < L; ++t) {
+            if (t % CKPT == 0) memcpy(ck + (size_t)(t / CKPT) * SS, S, sizeof(double) * SS);
+            gate_step(a, qo, vo, t, S);
+        }
+        free(S);
+    }
+
+    /* Gate branch, walked backwards block by block. */
+    for (int c = nck - 1; c >= 0; --c) {
+        const int t0 = c * CKPT, t1 = (t0 + CKPT < L) ? t0 + CKPT : L;
+        memcpy(blk, ck + (size_t)c * SS, sizeof(double) * SS);
+        for (int t = t0; t < t1; ++t) {
+            memcpy(blk + (size_t)(t - t0 + 1) * SS, blk + (size_t)(t - t0) * SS, sizeof(double) * SS);
+            gate_step(a, qo, vo, t, blk + (size_t)(t - t0 + 1) * SS);
+        }
+        for (int t = t1 - 1; t >= t0; --t) {
+            const double *St = blk + (size_t)(t - t0 + 1) * SS, *Sp = blk + (size_t)(t - t0) * SS;
+            for (int i = 0; i < dk; ++i) qt[i] = ld(a->dtype, a->q, qo + (size_t)t * dk + i);
+            for (int j = 0; j < dv; ++j) dyt[j] = a->dy[vo + (size_t)t * dv + j];
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0;
+                for (int j = 0; j < dv; ++j) {
+                    G[(size_t)i * dv + j] += qt[i] * dyt[j];
+                    acc += dyt[j] * St[(size_t)i * dv + j];
+                }
+                a->dq[qo + (size_t)t * dk + i] += acc;
+            }
+            for (int i = 0; i < dk; ++i) {
+                double acc_k = 0, acc_g = 0;
+                for (int j = 0; j < dv; ++j) {
+                    acc_k += G[(size_t)i * dv + j] * ld(a->dtype, a->v, vo + (size_t)t * dv + j);
+                    acc_g += G[(size_t)i * dv + j] * Sp[(size_t)i * dv + j];
+                }
+                a->dk_[qo + (size_t)t * dk + i] += acc_k;
+                const double gi = ld(a->dtype, a->g, qo + (size_t)t * dk + i);
+                const double sg = exp(oracle_log_sigmoid(gi)), sgn = exp(oracle_log_sigmoid(-gi));
+                a->dg[qo + (size_t)t * dk + i] = MUT(13) ? acc_g * sg : acc_g * sg * sgn;
+            }
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0;
+                for (int i = 0; i < dk; ++i)
+                    acc += ld(a->dtype, a->k, qo + (size_t)t * dk + i) * G[(size_t)i * dv + j];
+                a->dv_[vo + (size_t)t * dv + j] += acc;
+            }
+            if (!MUT(12)) /* (mutant 12 forgets to decay the state gradient) */
+                for (int i = 0; i < dk; ++i) {
+                    double gam = exp(oracle_log_sigmoid(ld(a->dtype, a->g, qo + (size_t)t * dk + i)));
+                    for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] *= gam;
+                }
+        }
+    }
+
+    /* Anchor branch, token by token (no recurrence). */
+    for (int t = 0; t < L; ++t) {
+        for (int i = 0; i < dk; ++i) qt[i] = ld(a->dtype, a->q, qo + (size_t)t * dk + i);
+        for (int j = 0; j < dv; ++j) dyt[j] = a->dy[vo + (size_t)t * dv + j];
+        int p0 = t - w + 1;
+        if (p0 < 0) p0 = 0;
+        const int n = t - p0 + 1;
+        double M = -INFINITY;
+        for (int c = 0; c < n; ++c) {
+            double s = 0;
+            for (int i = 0; i < dk; ++i) s += qt[i] * ld(a->dtype, a->k, qo + (size_t)(p0 + c) * dk + i);
+            sc[c] = s;
+            if (s > M) M = s;
+        }
+        for (int j = 0; j < m; ++j) {
+            double s = 0;
+            for (int i = 0; i < dk; ++i) s += qt[i] * ld(a->dtype, a->mu, ((size_t)h * m + j) * dk + i);
+            sc[n + j] = s;
+            if (s > M) M = s;
+        }
+        double Z = 0;
+        for (int c = 0; c < n + m; ++c) Z += exp(sc[c] - M);
+        for (int j = 0; j < dv; ++j) ya[j] = 0;
+        for (int c = 0; c < n; ++c) {
+            const double pr = exp(sc[c] - M) / Z;
+            for (int j = 0; j < dv; ++j) ya[j] += pr * ld(a->dtype, a->v, vo + (size_t)(p0 + c) * dv + j);
+        }
+        for (int j = 0; j < dv; ++j) dalpha += dyt[j] * ya[j];
+        /* dp_s = dya . v_s with dya = alpha dy_t; psum = sum_s p_s dp_s = dya . ya. */
+        double psum = 0;
+        for (int j = 0; j < dv; ++j) psum += a->alpha * dyt[j] * ya[j];
+        for (int c = 0; c < n; ++c) {
+            const int s = p0 + c;
+            const double pr = exp(sc[c] - M) / Z;
+            double dp = 0;
+            for (int j = 0; j < dv; ++j) {
+                const double vs = ld(a->dtype, a->v, vo + (size_t)s * dv + j);
+                dp += a->alpha * dyt[j] * vs;
+                a->dv_[vo + (size_t)s * dv + j] += pr * (MUT(16) ? dyt[j] : a->alpha * dyt[j]);
+            }
+            const double da = MUT(14) ? pr * dp : pr * (dp - psum);
+            for (int i = 0; i < dk; ++i) {
+                a->dq[qo + (size_t)t * dk + i] += da * ld(a->dtype, a->k, qo + (size_t)s * dk + i);
+                a->dk_[qo + (size_t)s * dk + i] += da * qt[i];
+            }
+        }
+        if (!MUT(15)) /* (mutant 15 drops the sinks' gradient) */
+            for (int j = 0; j < m; ++j) {
+                const double dc = exp(sc[n + j] - M) / Z * (0.0 - psum);
+                for (int i = 0; i < dk; ++i) {
+                    a->dq[qo + (size_t)t * dk + i] += dc * ld(a->dtype, a->mu, ((size_t)h * m + j) * dk + i);
+                    dmu[(size_t)j * dk + i] += dc * qt[i];
+                }
+            }
+    }
+    a->dalpha[u] = dalpha;
+    free(ck); free(blk); free(G); free(qt); free(dyt); free(ya); free(sc);
+}
+
+static void *backward_worker(void *p)
+{
+    const bwd_args *a = p;
+    for (int u = a->u_begin; u < a->u_end; ++u)
+        backward_unit(a, u);
+    return NULL;
+}
+
+/*
+ * oracle_backward: gradients of the operator over U = n_units (batch, head)
+ * units that start from the empty state.  Inputs as oracle_forward; dy
+ * [U][L][dv] fp64.  Outputs (fp64): dq, dk, dg [U][L][dk], dv [U][L][dv],
+ * dmu [U][m][dk] and dalpha [U], the last two per unit (the caller sums
+ * dmu over the batch for each head and dalpha over all units).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_backward(int dtype, const void *q, const void *k, const void *v, const void *g,
+                    const void *mu, double alpha, int n_units, int unit0, int H, int L,
+                    int dk, int dv, int w, int m, const double *dy,
+                    double *dq, double *dk_out, double *dv_out, double *dg, double *dmu,
+                    double *dalpha, int nthreads)
+{
+    if (n_units < 0 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0 || H < 1) return -1;
+    if ((dtype != ORACLE_F32 && dtype != ORACLE_BF16) || (m > 0 && !mu)) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n_units) nthreads = n_units > 0 ? n_units : 1;
+    bwd_args base = {dtype, q, k, v, g, mu, alpha, H, L, dk, dv, w, m, dy, dq, dk_out, dv_out, dg,
+                     dmu, dalpha, unit0, 0, 0};
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    bwd_args *args = malloc(sizeof(bwd_args) * nthreads);
+    for (int i = 0; i < nthreads; ++i) {
+        args[i] = base;
+        args[i].u_begin = (int)((long long)n_units * i / nthreads);
+        args[i].u_end = (int)((long long)n_units * (i + 1) / nthreads);
+        pthread_create(&th[i], NULL, backward_worker, &args[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th); free(args);
+    return 0;
+}

@@ -56,6 +56,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
         lib.oracle_decode_step.restype = I
         lib.oracle_gla_product_form.argtypes = [I, P, P, P, P, I, I, I, P, P]
         lib.oracle_gla_product_form.restype = I
+        lib.oracle_backward.argtypes = [I, P, P, P, P, P, D, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, I]
+        lib.oracle_backward.restype = I
         lib.oracle_log_sigmoid.argtypes = [D]
         lib.oracle_log_sigmoid.restype = D
         _libs[path] = lib
@@ -190,6 +192,50 @@ def decode_step(q, k, v, g, mu, alpha, st: dict, *, lib=None):
     if rc != 0:
         raise ValueError("oracle_decode_step rejected its arguments")
     return y
+
+
+def backward(q, k, v, g, mu, alpha, w, dy, *, threads=None, lib=None) -> dict:
+    """Gradients of sum(dy * y) for [B,H,L,d] inputs (or [U,L,d] units, H
+    from mu) that start from the empty state.
+
+    Returns fp64 tensors: dq, dk, dv, dg shaped like the inputs, dmu [H,m,dk]
+    (summed over the batch) and dalpha (a 0-d tensor, summed over all units).
+    """
+    lib = lib or load()
+    dt = _code(q)
+    lead = q.shape[:-2]
+    L, dk = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    H, m = mu.shape[0], mu.shape[1]
+    U = 1
+    for s_ in lead:
+        U *= s_
+    tensors = []
+
+    def keep(t):
+        t, p = _c(t)
+        tensors.append(t)
+        return p
+
+    pq, pk, pv, pg = keep(q), keep(k), keep(v), keep(g)
+    pmu = keep(mu) if m > 0 else None
+    pdy = keep(dy.double())
+    dq = torch.empty(*lead, L, dk, dtype=torch.float64)
+    dk_ = torch.empty_like(dq)
+    dg = torch.empty_like(dq)
+    dv_ = torch.empty(*lead, L, dv, dtype=torch.float64)
+    dmu_u = torch.empty(U, m, dk, dtype=torch.float64)
+    dalpha_u = torch.empty(U, dtype=torch.float64)
+    rc = lib.oracle_backward(dt, pq, pk, pv, pg, pmu, float(alpha), U, 0, H, L, dk, dv, int(w), m, pdy,
+                             ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk_.data_ptr()),
+                             ctypes.c_void_p(dv_.data_ptr()), ctypes.c_void_p(dg.data_ptr()),
+                             ctypes.c_void_p(dmu_u.data_ptr()), ctypes.c_void_p(dalpha_u.data_ptr()),
+                             threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
+    # unit u = b * H + h: sum dmu over the batch for each head
+    dmu = dmu_u.reshape(U // H if H else 0, H, m, dk).sum(0) if U else torch.zeros(H, m, dk, dtype=torch.float64)
+    return {"dq": dq, "dk": dk_, "dv": dv_, "dg": dg, "dmu": dmu, "dalpha": dalpha_u.sum()}
 
 
 def gla_product_form(q, k, v, g, S0=None, *, lib=None):

@@ -236,6 +236,111 @@ def pin_sink_free_weights_sum_to_one(lib):
     assert float(ya.max()) < 1.0
 
 
+# --- backward ----------------------------------------------------------------
+
+def _grid_inputs(seed, B, H, L, d, m):
+    """fp32 inputs on a 2^-8 grid in [-2, 2] (g in [-3, 3]), so that x +- h
+    stays exact in fp32 for the step sizes used below."""
+    gen = _gen(seed)
+
+    def grid(shape, scale):
+        return (torch.round(torch.rand(*shape, generator=gen) * 2 * scale * 256 - scale * 256) / 256).float()
+
+    return (grid((B, H, L, d), 1.0), grid((B, H, L, d), 1.0), grid((B, H, L, d), 2.0), grid((B, H, L, d), 3.0),
+            grid((H, m, d), 1.0))
+
+
+def _loss(q, k, v, g, mu, alpha, w, dy, lib):
+    return float((O.forward(q, k, v, g, mu, alpha, w, lib=lib) * dy).sum())
+
+
+def _fd_grad(x, f, h):
+    """Central differences of f at every element of x (a CPU fp32 tensor),
+    Richardson-extrapolated over steps h and h/2 (error O(h^4))."""
+    out = torch.empty(x.shape, dtype=f64)
+    flat = x.reshape(-1)
+    for i in range(flat.numel()):
+        x0 = float(flat[i])
+        vals = []
+        for step in (h, h / 2):
+            flat[i] = x0 + step
+            fp = f()
+            flat[i] = x0 - step
+            fm = f()
+            vals.append((fp - fm) / (2 * step))
+        flat[i] = x0
+        out.reshape(-1)[i] = (4 * vals[1] - vals[0]) / 3
+    return out
+
+
+def pin_backward_vs_finite_differences(lib):
+    # Gradients of sum(dy * y) against finite differences of the forward
+    # oracle, element by element, for every input, mu and alpha.
+    for (seed, L, d, w, m) in ((101, 9, 4, 3, 2), (102, 70, 3, 5, 1)):
+        B, H, alpha = 1, 2, 0.7
+        q, k, v, g, mu = _grid_inputs(seed, B, H, L, d, m)
+        dy = torch.randn(B, H, L, d, generator=_gen(seed + 1), dtype=f64)
+        got = O.backward(q, k, v, g, mu, alpha, w, dy, lib=lib)
+        f = lambda: _loss(q, k, v, g, mu, alpha, w, dy, lib)  # noqa: E731
+        h = 2.0 ** -7
+        for name, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dmu", mu)):
+            _close(got[name], _fd_grad(x, f, h), 1e-7, f"{name} vs finite differences (L={L})")
+        da = [(_loss(q, k, v, g, mu, alpha + st, w, dy, lib) - _loss(q, k, v, g, mu, alpha - st, w, dy, lib))
+              / (2 * st) for st in (h, h / 2)]
+        _close(got["dalpha"].reshape(1), torch.tensor([(4 * da[1] - da[0]) / 3], dtype=f64), 1e-9,
+               "dalpha vs finite differences")
+
+
+def _autograd_forward(q, k, v, g, mu, alpha, w):
+    """The operator in plain fp64 PyTorch ops, one token at a time (a second,
+    separately written forward, differentiated by autograd)."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    S = torch.zeros(B, H, dk, dv, dtype=f64)
+    ys = []
+    for t in range(L):
+        gam = torch.sigmoid(g[:, :, t])
+        S = gam[..., None] * S + k[:, :, t, :, None] * v[:, :, t, None, :]
+        yg = torch.einsum("bhi,bhij->bhj", q[:, :, t], S)
+        lo = max(0, t - w + 1)
+        kw, vw = k[:, :, lo:t + 1], v[:, :, lo:t + 1]
+        a = torch.einsum("bhi,bhsi->bhs", q[:, :, t], kw)
+        c = torch.einsum("bhi,hji->bhj", q[:, :, t], mu)
+        logits = torch.cat([a, c], dim=-1)
+        p = torch.softmax(logits, dim=-1)[..., : a.shape[-1]]
+        ya = torch.einsum("bhs,bhsj->bhj", p, vw)
+        ys.append(yg + alpha * ya)
+    return torch.stack(ys, dim=2)
+
+
+def pin_backward_vs_autograd(lib):
+    # A longer sequence (crossing the oracle's internal checkpoints) against
+    # autograd through the plain PyTorch forward above.
+    B, H, L, d, w, m, alpha = 1, 2, 130, 8, 7, 3, 0.8
+    q, k, v, g, mu = _qkvg(111, B, H, L, d, d, m=m, g_mean=1.0, g_std=2.0)
+    dy = torch.randn(B, H, L, d, generator=_gen(112), dtype=f64)
+    got = O.backward(q, k, v, g, mu, alpha, w, dy, lib=lib)
+    leaves = [t.double().requires_grad_(True) for t in (q, k, v, g, mu)]
+    al = torch.tensor(alpha, dtype=f64, requires_grad=True)
+    y = _autograd_forward(*leaves, al, w)
+    (y * dy).sum().backward()
+    for name, t in zip(("dq", "dk", "dv", "dg", "dmu"), leaves):
+        _close(got[name], t.grad, 1e-10, f"{name} vs autograd")
+    _close(got["dalpha"].reshape(1), al.grad.reshape(1), 1e-10, "dalpha vs autograd")
+
+
+def pin_backward_open_gates_have_no_gate_gradient(lib):
+    # sigmoid(g) = 1 to fp64 precision (g = 1e4): the gate does not move, so
+    # dg is exactly 0 whatever dy is.
+    B, H, L, d = 1, 1, 20, 4
+    q, k, v, g, mu = _qkvg(121, B, H, L, d, d, m=2)
+    g = torch.full_like(g, 1e4)
+    dy = torch.randn(B, H, L, d, generator=_gen(122), dtype=f64)
+    got = O.backward(q, k, v, g, mu, 1.0, 4, dy, lib=lib)
+    assert float(got["dg"].abs().max()) == 0.0
+    assert float(got["dq"].abs().max()) > 0.0
+
+
 PINS = [
     pin_log_sigmoid_vs_scipy,
     pin_recurrence_equals_product_form,
@@ -249,4 +354,7 @@ PINS = [
     pin_split_prefill_equals_whole,
     pin_decode_continues_prefill,
     pin_sink_free_weights_sum_to_one,
+    pin_backward_vs_finite_differences,
+    pin_backward_vs_autograd,
+    pin_backward_open_gates_have_no_gate_gradient,
 ]

@@ -12,7 +12,7 @@ import pytest
 from oracle import oracle as O
 from tests.oracle_pins import PINS
 
-N_MUTANTS = 11
+N_MUTANTS = 16
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
