@@ -5,6 +5,7 @@ C ABI of ``include/lizard_attn.h``.
 from .lizard_attn import (  # noqa: F401
     LizardError,
     LizardState,
+    lizard_attn_backward,
     lizard_attn_decode_step,
     lizard_attn_prefill,
     lizard_attn_prefill_continue,

@@ -4,8 +4,8 @@
 // prefill_ws.cuh (bf16, d = 128, w <= 65: warp-specialised tensor cores, with
 // the segment pre-pass of prefill_state.cuh), prefill_tc.cuh (bf16, d = 128,
 // w > 65: tensor cores), prefill_simt.cuh (fp32 and d = 64: CUDA cores, exact
-// fp32), prefill_cont.cuh (start position of a continued prompt) and the
-// state initialiser below.  Declarations and the contract of every entry point are
+// fp32), prefill_cont.cuh (start position of a continued prompt),
+// backward_simt.cuh (gradients) and the state initialiser below.  Declarations and the contract of every entry point are
 // in include/lizard_attn.h.
 #include <cuda_runtime.h>
 
@@ -22,6 +22,7 @@
 #include "prefill_ws.cuh"
 #include "prefill_state.cuh"
 #include "prefill_cont.cuh"
+#include "backward_simt.cuh"
 
 namespace lizard {
 
@@ -275,6 +276,45 @@ static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
     return launch_status();
 }
 
+// Gradients: the two-sweep kernel over every unit, then the reduction of the
+// per-unit d mu and d alpha parts.  Scratch in stream-ordered memory.
+template <typename T, int D>
+static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha, cudaStream_t s)
+{
+    const size_t units = (size_t)ba.B * ba.H;
+    const size_t xq_bytes = units * ba.L * D * sizeof(float);
+    const size_t row_bytes = units * ba.L * sizeof(float);
+    const size_t dmu_bytes = units * ba.m * D * sizeof(float);
+    const size_t bytes = xq_bytes + 2 * row_bytes + dmu_bytes + units * sizeof(float);
+    uint8_t *scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LIZARD_ERR_CUDA;
+    }
+    ba.xq = reinterpret_cast<float *>(scratch);
+    ba.lse = reinterpret_cast<float *>(scratch + xq_bytes);
+    ba.drow = reinterpret_cast<float *>(scratch + xq_bytes + row_bytes);
+    ba.dmu_part = reinterpret_cast<float *>(scratch + xq_bytes + 2 * row_bytes);
+    ba.dalpha_part = reinterpret_cast<float *>(scratch + xq_bytes + 2 * row_bytes + dmu_bytes);
+    lizard_status rc = LIZARD_OK;
+    const size_t smem = backward_simt_smem_bytes<D>(ba.w, ba.m);
+    auto kern = backward_simt_kernel<T, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        rc = LIZARD_ERR_CUDA;
+    } else {
+        kern<<<(unsigned)units, BW_THREADS, smem, s>>>(ba);
+        rc = launch_status();
+    }
+    if (rc == LIZARD_OK) {
+        const int mD = ba.m * D, n = ba.H * mD;
+        backward_reduce_kernel<<<n > 0 ? (n + 255) / 256 : 1, 256, 0, s>>>(ba.dmu_part, ba.dalpha_part, ba.B, ba.H,
+                                                                           mD, dmu, dalpha);
+        rc = launch_status();
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
+    return rc;
+}
+
 // ---------------------------------------------------------------- allocation-free prefill
 // Segment states of lizard_attn_prefill_noalloc: a fixed array in device
 // memory, held by every GPU that loads this library until the process ends.
@@ -425,6 +465,38 @@ lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const v
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
                          : launch_prefill<__nv_bfloat16, 64>(pa, s);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
+}
+
+lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
+                                   float alpha, int B, int H, int L, int dk, int dv, int w, int m, lizard_dtype dtype,
+                                   const void *dy, void *dq, void *dk_out, void *dv_out, void *dg, float *dmeta_k,
+                                   float *dalpha, lizard_stream_t stream)
+{
+    if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
+    if (B < 0 || H < 1 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0) return LIZARD_ERR_INVALID_ARG;
+    if (L > 0 && B > 0 && (!q || !k || !v || !g || !dy || !dq || !dk_out || !dv_out || !dg))
+        return LIZARD_ERR_INVALID_ARG;
+    if (m > 0 && (!meta_k || !dmeta_k)) return LIZARD_ERR_INVALID_ARG;
+    if (!dalpha || (reinterpret_cast<uintptr_t>(dalpha) & 3u)) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dy) || !aligned16(dq) ||
+        !aligned16(dk_out) || !aligned16(dv_out) || !aligned16(dg) || (m > 0 && (!aligned16(meta_k) || !aligned16(dmeta_k))))
+        return LIZARD_ERR_INVALID_ARG;
+    if (dk != dv || (dk != 64 && dk != 128)) return LIZARD_ERR_UNSUPPORTED;
+    if (w > LIZARD_MAX_WINDOW || m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B == 0 || L == 0) {  // no token: the parameter gradients are zero
+        if (cudaMemsetAsync(dalpha, 0, sizeof(float), s) != cudaSuccess) return LIZARD_ERR_CUDA;
+        if (m > 0 && cudaMemsetAsync(dmeta_k, 0, sizeof(float) * H * m * dk, s) != cudaSuccess) return LIZARD_ERR_CUDA;
+        return LIZARD_OK;
+    }
+    BackwardArgs ba{q, k, v, g, meta_k, dy, dq, dk_out, dv_out, dg, alpha, B, H, L, w, m,
+                    nullptr, nullptr, nullptr, nullptr, nullptr};
+    float *dmu = m > 0 ? dmeta_k : nullptr;
+    if (dtype == LIZARD_BF16)
+        return dk == 128 ? launch_backward<__nv_bfloat16, 128>(ba, dmu, dalpha, s)
+                         : launch_backward<__nv_bfloat16, 64>(ba, dmu, dalpha, s);
+    return dk == 128 ? launch_backward<float, 128>(ba, dmu, dalpha, s) : launch_backward<float, 64>(ba, dmu, dalpha, s);
 }
 
 lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,

@@ -24,7 +24,7 @@ LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
 EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
-           "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string")
+           "lizard_attn_backward", "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string")
 
 
 class LizardError(RuntimeError):
@@ -63,6 +63,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lizard_attn_prefill_continue.restype = I
         lib.lizard_attn_prefill_noalloc.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
         lib.lizard_attn_prefill_noalloc.restype = I
+        lib.lizard_attn_backward.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+        lib.lizard_attn_backward.restype = I
         lib.lizard_attn_decode_step.argtypes = [P, P, P, P, P, F, I, P, SP, P]
         lib.lizard_attn_decode_step.restype = I
         lib.lizard_check_device_status.argtypes = [P]
@@ -180,6 +182,26 @@ def lizard_attn_prefill_noalloc(q, k, v, g, meta_k, alpha, w, y=None, state: Liz
         ctypes.byref(st) if st is not None else None, _stream(stream))
     _check(rc, "lizard_attn_prefill_noalloc")
     return y
+
+
+def lizard_attn_backward(q, k, v, g, meta_k, alpha, w, dy, stream=None):
+    """Gradients of sum(dy * y) through the operator over [B,H,L,d] tensors
+    that start from the empty state.  Returns (dq, dk, dv, dg, dmeta_k,
+    dalpha): the first four in the input dtype, dmeta_k [H,m,dk] fp32 (None
+    when m == 0) and dalpha a 0-d fp32 tensor, all on the inputs' device."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    m = meta_k.shape[1] if meta_k is not None else 0
+    dq, dk_, dg = (torch.empty_like(q) for _ in range(3))
+    dv_ = torch.empty_like(v)
+    dmeta = torch.empty(H, m, dk, dtype=torch.float32, device=q.device) if m > 0 else None
+    dalpha = torch.empty((), dtype=torch.float32, device=q.device)
+    rc = library().lizard_attn_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha),
+        B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(dy), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg),
+        _ptr(dmeta) if m > 0 else None, _ptr(dalpha), _stream(stream))
+    _check(rc, "lizard_attn_backward")
+    return dq, dk_, dv_, dg, dmeta, dalpha
 
 
 def lizard_attn_decode_step(q, k, v, g, meta_k, alpha, state: LizardState, y=None, stream=None) -> torch.Tensor:

@@ -183,6 +183,31 @@ LIZARD_API lizard_status lizard_attn_prefill_noalloc(const void *q, const void *
                                           lizard_stream_t stream);
 
 /*
+ * lizard_attn_backward: gradients of a scalar loss through the operator over
+ * a prompt that starts from the empty state (training), given dy = dLoss/dy.
+ * The gate (gist.science/de section 2 item 1, gamma = sigmoid(g)), the
+ * meta-memory keys (item 2) and alpha (item 3) are trained along with the
+ * inputs, so every one of them gets a gradient:
+ *   q, k, g, v, meta_k, alpha, B..m, dtype   as lizard_attn_prefill
+ *   dy       [B][H][L][dv]  dtype   upstream gradient
+ *   dq, dk, dg [B][H][L][dk] dtype, dv [B][H][L][dv] dtype   written
+ *   dmeta_k  [H][m][dk]     fp32    written (summed over the batch); may be
+ *                                   NULL when m == 0
+ *   dalpha   one fp32 value         written (summed over everything); 4-byte
+ *                                   aligned
+ * Gradients are computed in fp32 from the stored input bits (every gate
+ * value is handled: all exponents the kernel takes are <= 0) and rounded
+ * to dtype once.  The call allocates its scratch on `stream` (cudaMallocAsync
+ * / cudaFreeAsync): 4 (L dk + 2 L + m dk + 1) bytes per (batch, head) unit.
+ * L == 0 or B == 0 writes zero dmeta_k and dalpha and nothing else.
+ */
+LIZARD_API lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, const void *g,
+                                   const void *meta_k, float alpha, int B, int H, int L, int dk, int dv,
+                                   int w, int m, lizard_dtype dtype, const void *dy, void *dq, void *dk_out,
+                                   void *dv_out, void *dg, float *dmeta_k, float *dalpha,
+                                   lizard_stream_t stream);
+
+/*
  * lizard_attn_decode_step: one new token for each of st->B sequences and
  * st->H heads, continuing from `st` (updated in place).
  *   q, k, g  [B][H][dk]  st->dtype;  v [B][H][dv];  meta_k [H][m][dk]

@@ -133,6 +133,7 @@ def test_state_init_rejects(lib):
 def test_binding_names_match_the_c_abi():
     import hybrid_gated_linear_attn_b300 as pkg
     for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
+                 "lizard_attn_backward",
                  "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string"):
         assert callable(getattr(pkg, name))
 
@@ -159,3 +160,21 @@ def test_continue_empty_calls_launch_nothing(lib):
     # No new token, or no sequence: the state stays as it is and nothing runs.
     assert cont(lib, q=None, k=None, v=None, g=None, y=None, L=0) == OK
     assert cont(lib, st=state(Bn=0)) == OK
+
+
+def backward(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128, dv=128, w=64, m=4,
+             dtype=LA.LIZARD_BF16, dy=A, dq=A, dko=A, dvo=A, dg=A, dmu=A, dal=A):
+    return lib.lizard_attn_backward(q, k, v, g, mu, alpha, Bn, H, L, dk, dv, w, m, dtype, dy, dq, dko, dvo, dg,
+                                    dmu, dal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), INVALID), (dict(dy=None), INVALID), (dict(dq=None), INVALID), (dict(dg=None), INVALID),
+    (dict(dvo=None), INVALID), (dict(mu=None), INVALID), (dict(dmu=None), INVALID), (dict(dal=None), INVALID),
+    (dict(dal=A + 2), INVALID), (dict(dy=MIS), INVALID), (dict(dmu=MIS), INVALID),
+    (dict(dtype=7), INVALID), (dict(w=0), INVALID), (dict(m=-1), INVALID), (dict(L=-1), INVALID),
+    (dict(H=0), INVALID), (dict(dk=96, dv=96), UNSUPPORTED), (dict(dk=128, dv=64), UNSUPPORTED),
+    (dict(w=LA.LIZARD_MAX_WINDOW + 1), UNSUPPORTED), (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
+])
+def test_backward_rejects(lib, kw, code):
+    assert backward(lib, **kw) == code
