@@ -23,6 +23,7 @@
 #include "prefill_state.cuh"
 #include "prefill_cont.cuh"
 #include "backward_simt.cuh"
+#include "backward_tc.cuh"
 
 namespace lizard {
 
@@ -315,6 +316,73 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
     return rc;
 }
 
+// Gradients on the tensor cores (bf16, d = 128, w <= 65): the chunk states
+// and state gradients, then the query-side and key-side kernels over every
+// (unit, chunk).  d mu and d alpha are accumulated, so they start at zero.
+static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, float *dalpha, cudaStream_t s)
+{
+    const int units = ba.B * ba.H, L = ba.L, nch = (L + bwdtc::C - 1) / bwdtc::C;
+    const size_t D = bwdtc::D;
+    const size_t st_bytes = (size_t)units * nch * D * D * sizeof(__nv_bfloat16);
+    const size_t xq_bytes = (size_t)units * L * D * sizeof(float);
+    const size_t row_bytes = ((size_t)units * L * sizeof(float) + 255) & ~(size_t)255;
+    uint8_t *scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LIZARD_ERR_CUDA;
+    }
+    __nv_bfloat16 *Sb = reinterpret_cast<__nv_bfloat16 *>(scratch);
+    __nv_bfloat16 *Ha = reinterpret_cast<__nv_bfloat16 *>(scratch + st_bytes);
+    float *xq = reinterpret_cast<float *>(scratch + 2 * st_bytes);
+    float *lse2 = reinterpret_cast<float *>(scratch + 2 * st_bytes + xq_bytes);
+    float *drow = reinterpret_cast<float *>(scratch + 2 * st_bytes + xq_bytes + row_bytes);
+    lizard_status rc = LIZARD_OK;
+    CUtensorMap tq, tk, tv, tg, tdy, tS, tH;
+    if (!make_token_map(&tq, ba.q, units, L) || !make_token_map(&tk, ba.k, units, L) ||
+        !make_token_map(&tv, ba.v, units, L) || !make_token_map(&tg, ba.g, units, L) ||
+        !make_token_map(&tdy, ba.dy, units, L) || !make_token_map(&tS, Sb, units * nch, (int)D) ||
+        !make_token_map(&tH, Ha, units * nch, (int)D))
+        rc = LIZARD_ERR_CUDA;
+    if (rc == LIZARD_OK && cudaMemsetAsync(dalpha, 0, sizeof(float), s) != cudaSuccess) rc = LIZARD_ERR_CUDA;
+    if (rc == LIZARD_OK && dmu && cudaMemsetAsync(dmu, 0, sizeof(float) * ba.H * ba.m * D, s) != cudaSuccess)
+        rc = LIZARD_ERR_CUDA;
+    if (rc == LIZARD_OK) {
+        bwdtc::StatesArgs sa{Sb, Ha, L, nch};
+        if (cudaFuncSetAttribute(bwdtc::chunk_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwdtc::ST_SMEM) != cudaSuccess)
+            rc = LIZARD_ERR_CUDA;
+        else {
+            bwdtc::chunk_states_kernel<<<dim3(units, 2), bwdtc::THREADS, bwdtc::ST_SMEM, s>>>(tg, tk, tv, tq, tdy, sa);
+            rc = launch_status();
+        }
+    }
+    if (rc == LIZARD_OK) {
+        bwdtc::QueryArgs qa{static_cast<const __nv_bfloat16 *>(ba.mu), static_cast<const __nv_bfloat16 *>(ba.k),
+                            static_cast<__nv_bfloat16 *>(ba.dq), xq, lse2, drow, dmu, dalpha, ba.alpha, ba.H, L,
+                            ba.w, ba.m, nch};
+        if (cudaFuncSetAttribute(bwdtc::bwd_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwdtc::QO_SMEM) != cudaSuccess)
+            rc = LIZARD_ERR_CUDA;
+        else {
+            bwdtc::bwd_query_kernel<<<units * nch, bwdtc::THREADS, bwdtc::QO_SMEM, s>>>(tq, tk, tv, tg, tdy, tS, qa);
+            rc = launch_status();
+        }
+    }
+    if (rc == LIZARD_OK) {
+        bwdtc::KeyArgs ka{Sb, xq, lse2, drow, static_cast<__nv_bfloat16 *>(ba.dk), static_cast<__nv_bfloat16 *>(ba.dv),
+                          static_cast<__nv_bfloat16 *>(ba.dg), ba.alpha, L, ba.w, nch};
+        if (cudaFuncSetAttribute(bwdtc::bwd_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwdtc::KO_SMEM) != cudaSuccess)
+            rc = LIZARD_ERR_CUDA;
+        else {
+            bwdtc::bwd_key_kernel<<<units * nch, bwdtc::THREADS, bwdtc::KO_SMEM, s>>>(tq, tk, tv, tg, tdy, tH, ka);
+            rc = launch_status();
+        }
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
+    return rc;
+}
+
 // ---------------------------------------------------------------- allocation-free prefill
 // Segment states of lizard_attn_prefill_noalloc: a fixed array in device
 // memory, held by every GPU that loads this library until the process ends.
@@ -493,6 +561,7 @@ lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, 
     BackwardArgs ba{q, k, v, g, meta_k, dy, dq, dk_out, dv_out, dg, alpha, B, H, L, w, m,
                     nullptr, nullptr, nullptr, nullptr, nullptr};
     float *dmu = m > 0 ? dmeta_k : nullptr;
+    if (dtype == LIZARD_BF16 && dk == 128 && w <= 65) return launch_backward_tc(ba, dmu, dalpha, s);
     if (dtype == LIZARD_BF16)
         return dk == 128 ? launch_backward<__nv_bfloat16, 128>(ba, dmu, dalpha, s)
                          : launch_backward<__nv_bfloat16, 64>(ba, dmu, dalpha, s);

@@ -59,7 +59,11 @@ def _check(inp, w):
             errs["dmu"] = rel_l2(dmu, ref["dmu"])
         else:  # alpha = 0: the sinks get no gradient at all
             errs["dmu"] = 0.0 if float(dmu.abs().max()) == 0.0 else float("inf")
-    errs["dalpha"] = abs(float(dal) - float(ref["dalpha"])) / max(abs(float(ref["dalpha"])), 1e-30)
+    # d alpha = sum_t dy_t . ya_t: a sum of terms of both signs, each computed
+    # to relative accuracy tol, so its error is bounded by tol * sum |dy ya|.
+    _, _, ya = O.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], w, branches=True)
+    scale = float((inp["dy"].double() * ya).abs().sum())
+    errs["dalpha"] = abs(float(dal) - float(ref["dalpha"])) / max(scale, 1e-30)
     bad = {n: e for n, e in errs.items() if not e <= tol}
     assert not bad, f"rel L2 above {tol}: {bad} (all: {errs})"
     return errs
@@ -81,6 +85,20 @@ CASES = [
     ("f32_alpha_zero", "f32", 1, 2, 80, 64, 16, 4, 3.0, 1.0, 0.0),
     ("bf16_d64_w100", "bf16", 2, 3, 257, 64, 100, 4, 3.0, 1.0, 1.0),
     ("bf16_mixed_decay", "bf16", 1, 3, 333, 128, 48, 4, -1.0, 3.0, 0.8),
+    # tensor-core path (bf16, d = 128, w <= 65): chunk boundaries, ragged
+    # tails, wide-span chunks on the exact path, windows 1 .. 65
+    ("tc_one_chunk", "bf16", 2, 2, 64, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_chunk_plus_one", "bf16", 1, 2, 65, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_single_token", "bf16", 1, 2, 1, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_window_one", "bf16", 1, 2, 190, 128, 1, 3, 3.0, 1.0, 1.0),
+    ("tc_window_33", "bf16", 1, 2, 300, 128, 33, 2, 3.0, 1.0, 0.6),
+    ("tc_window_65_max_meta", "bf16", 1, 2, 260, 128, 65, 16, 3.0, 1.0, 1.0),
+    ("tc_no_meta", "bf16", 1, 2, 200, 128, 64, 0, 3.0, 1.0, 1.0),
+    ("tc_alpha_zero", "bf16", 1, 2, 150, 128, 64, 4, 3.0, 1.0, 0.0),
+    ("tc_wide_span_exact", "bf16", 1, 2, 300, 128, 64, 4, -8.0, 4.0, 1.0),
+    ("tc_strong_decay", "bf16", 1, 2, 256, 128, 64, 8, 0.0, 2.0, 0.5),
+    ("tc_open_gates", "bf16", 1, 2, 200, 128, 32, 4, 12.0, 0.5, 1.0),
+    ("tc_many_units", "bf16", 3, 8, 130, 128, 64, 4, 3.0, 1.0, 1.0),
 ]
 
 
