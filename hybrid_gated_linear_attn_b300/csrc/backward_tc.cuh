@@ -722,13 +722,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 const size_t row = (size_t)unit * L + c0 + t;
-                __nv_bfloat16 *dqp = a.dq + row * D + i0;
-                float *xqp = a.xq + row * D + i0;
+                uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    dqp[e] = __float2bfloat16_rn(gate[e] + __uint_as_float(qa[e]));
-                    xqp[e] = xg[e];
-                }
+                for (int e = 0; e < 16; e += 2)
+                    pk[e / 2] = f2_to_bf2(gate[e] + __uint_as_float(qa[e]), gate[e + 1] + __uint_as_float(qa[e + 1]));
+                uint4 *dqp = reinterpret_cast<uint4 *>(a.dq + row * D + i0);
+                dqp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dqp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                float4 *xqp = reinterpret_cast<float4 *>(a.xq + row * D + i0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) xqp[u] = make_float4(xg[4 * u], xg[4 * u + 1], xg[4 * u + 2], xg[4 * u + 3]);
             }
         }
     } while (false);
@@ -769,8 +772,8 @@ constexpr uint32_t KO_DSCN = KO_PN + TILE;      // score gradients, next chunk's
 constexpr uint32_t KO_DAT = KO_DSCN + TILE;     // tril(dy v^T) [t][s]
 constexpr uint32_t KO_AT = KO_DAT + TILE;       // tril(A) [t][s]
 constexpr uint32_t KO_B = KO_PC;
-constexpr uint32_t KO_VEC = KO_AT + TILE;       // r[128], b_last[128], tot[4][128]
-constexpr uint32_t KO_BAR = KO_VEC + (128 + 128 + 512) * 4;
+constexpr uint32_t KO_VEC = KO_AT + TILE;       // r[128], b_last[128], tot[4][128], E parts [2][128]
+constexpr uint32_t KO_BAR = KO_VEC + (128 + 128 + 512 + 256) * 4;
 constexpr uint32_t KO_TSLOT = KO_BAR + 3 * 8;
 constexpr uint32_t KO_SMEM = KO_TSLOT + 8 + 1024;
 static_assert(KO_SMEM <= 232448, "shared memory budget");
@@ -788,7 +791,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float *rv = reinterpret_cast<float *>(sm + KO_VEC), *blv = rv + 128, *tot = blv + 128;
+    float *rv = reinterpret_cast<float *>(sm + KO_VEC), *blv = rv + 128, *tot = blv + 128, *Ep = tot + 512;
     float *bk = reinterpret_cast<float *>(sm + KO_B);  // phase B: b [64][128]
     float *yo = reinterpret_cast<float *>(sm + KO_QN);  // after the gate products: k * dk_inter [64][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + KO_BAR);
@@ -847,6 +850,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3, hs = lane >> 4;
     const int t = 16 * quarter + (lane & 15);  // this thread's accumulator row
     const uint32_t tl = tmem + tlane(quarter);
+    // row statistics of this thread's query row (warps 0-3: this chunk,
+    // warps 4-7: the next chunk), fetched while the tiles load
+    const bool nxt = warp >= 4;
+    const int tq_row = nxt ? c0 + C + t : c0 + t;
+    const bool qrow_ok = nxt ? t < nn : t < n;
+    const float l2 = qrow_ok ? a.lse2[(size_t)unit * L + tq_row] : 0.f;
+    const float Dt = qrow_ok ? a.drow[(size_t)unit * L + tq_row] : 0.f;
     int unsafe = 0;
     do {
         if (!cta_wait(bar_in, 0)) break;
@@ -866,16 +876,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             commit();
         }
+        // the later chunks' share of dlog gamma needs sum_j Sb[c][i][j] H[i][j]
+        // (scaled by 2^{b_last} later): row i, columns 64 half .. + 63
+        {
+            const int i = tid & 127, half = tid >> 7;
+            const uint4 *Sp = reinterpret_cast<const uint4 *>(a.Sb + ((size_t)unit * nch + c) * D * D + (size_t)i * D +
+                                                              64 * half);
+            uint4 sv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sv[u] = Sp[u];
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint4 hv = *reinterpret_cast<const uint4 *>(sm + KO_H + half * 2 * TILE + sw128_offset(i, 16 * u));
+                const uint32_t sw[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w}, hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 s2 = bf2_to_f2(sw[e]), h2 = bf2_to_f2(hw[e]);
+                    acc = fmaf(s2.x, h2.x, acc);
+                    acc = fmaf(s2.y, h2.y, acc);
+                }
+            }
+            Ep[half * 128 + i] = acc;
+        }
         if (!mma_wait()) break;
         tc_fence_after();
         // ---- E1a: probabilities and score gradients (warps 0-3: this chunk's
         // rows; warps 4-7: the next chunk's rows), tril(dy v^T)
         {
-            const bool nxt = warp >= 4;
-            const int tg = nxt ? c0 + C + t : c0 + t;  // query position
-            const bool rowok = nxt ? t < nn : t < n;
-            const float l2 = rowok ? a.lse2[(size_t)unit * L + tg] : 0.f;
-            const float Dt = rowok ? a.drow[(size_t)unit * L + tg] : 0.f;
+            const int tg = tq_row;  // query position
+            const bool rowok = qrow_ok;
             // key s of this chunk is in row tg's window iff tg - w + 1 <= c0 + s <= tg
             const int slo = tg - w + 1 - c0, shi = tg - c0;
             uint32_t r[2][16], d[2][16];
@@ -1087,21 +1117,36 @@ __global__ void __launch_bounds__(THREADS, 1)
         {
             const int colh = warp >> 2;
             const bool rowok = t < n;
-            float term[2][16], tout[2][16];
-#pragma unroll 1
+            const size_t row = (size_t)unit * L + c0 + t;
+            float term[2][16];
+#pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int i0 = 64 * colh + 32 * jj + 16 * hs;
                 const uint32_t cofs = 64 * colh + 32 * jj;
                 uint32_t g1[16], g2[16], ka[16], vv[16];
+                float xqv[16];
+                if (rowok) {
+                    const float4 *xp = reinterpret_cast<const float4 *>(a.xq + row * D + i0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 x4 = xp[u];
+                        xqv[4 * u] = x4.x;
+                        xqv[4 * u + 1] = x4.y;
+                        xqv[4 * u + 2] = x4.z;
+                        xqv[4 * u + 3] = x4.w;
+                    }
+                }
                 tmem_ld16_x2<16>(tl + KT_G1 + cofs, g1);
                 tmem_ld16_x2<16>(tl + KT_G2 + cofs, g2);
                 tmem_ld16_x2<16>(tl + KT_DKA + cofs, ka);
                 tmem_ld16_x2<16>(tl + KT_DV + cofs, vv);
                 tmem_wait_ld();
-                const size_t row = (size_t)unit * L + c0 + t;
+                uint32_t dkp[8], dvp[8];
+                float dkv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int i = i0 + e;
+                    dkv[e] = 0.f;
                     if (rowok) {
                         const float bs = bk[t * D + i];
                         const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
@@ -1122,40 +1167,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                             kintra = kv * intra;
                         }
-                        a.dk[row * D + i] = __float2bfloat16_rn(inter + intra + __uint_as_float(ka[e]));
-                        a.dv[row * D + i] = __float2bfloat16_rn(__uint_as_float(vv[e]));
-                        term[jj][e] = a.xq[row * D + i] - kintra;
-                        tout[jj][e] = kv * inter;
+                        dkv[e] = inter + intra + __uint_as_float(ka[e]);
+                        term[jj][e] = xqv[e] - kintra;
+                        yo[t * D + i] = kv * inter;  // the QR / KL slot: read by M2b, which is done
                     } else {
                         term[jj][e] = 0.f;
-                        tout[jj][e] = 0.f;
+                        yo[t * D + i] = 0.f;
                     }
                 }
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    dkp[e / 2] = f2_to_bf2(dkv[e], dkv[e + 1]);
+                    dvp[e / 2] = f2_to_bf2(__uint_as_float(vv[e]), __uint_as_float(vv[e + 1]));
+                }
+                if (rowok) {
+                    uint4 *dkq = reinterpret_cast<uint4 *>(a.dk + row * D + i0);
+                    uint4 *dvq = reinterpret_cast<uint4 *>(a.dv + row * D + i0);
+                    dkq[0] = make_uint4(dkp[0], dkp[1], dkp[2], dkp[3]);
+                    dkq[1] = make_uint4(dkp[4], dkp[5], dkp[6], dkp[7]);
+                    dvq[0] = make_uint4(dvp[0], dvp[1], dvp[2], dvp[3]);
+                    dvq[1] = make_uint4(dvp[4], dvp[5], dvp[6], dvp[7]);
+                }
             }
-            __syncthreads();  // every read of b (and of QR / KL) is done
+            __syncthreads();  // every read of b is done
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i = 64 * colh + 32 * jj + 16 * hs + e;
-                    bk[t * D + i] = term[jj][e];
-                    yo[t * D + i] = tout[jj][e];
-                }
+                for (int e = 0; e < 16; ++e) bk[t * D + 64 * colh + 32 * jj + 16 * hs + e] = term[jj][e];
         }
         __syncthreads();
         // ---- dg = dlog gamma * sigmoid(-g)
         if (tid < D) {
             const int i = tid;
-            float E = 0.f;
-            {
-                const __nv_bfloat16 *Sp = a.Sb + ((size_t)unit * nch + c) * D * D + (size_t)i * D;
-                for (int j = 0; j < D; ++j) {
-                    const float hv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sm + KO_H + (j / 64) * 2 * TILE + sw128_offset(i, (j % 64) * 2)));
-                    E += __bfloat162float(Sp[j]) * hv;
-                }
-                E *= ex2(blv[i]);
-            }
+            const float E = (Ep[i] + Ep[128 + i]) * ex2(blv[i]);
             // forward exclusive prefix of k * dk_inter, in place
             float f = 0.f;
             for (int t2 = 0; t2 < n; ++t2) {

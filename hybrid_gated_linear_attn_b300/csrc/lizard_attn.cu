@@ -43,6 +43,45 @@ __global__ void state_init_kernel(float *S, size_t nS, uint4 *ring_k, uint4 *rin
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stream-ordered scratch from a memory pool this library owns, one per
+// device.  Its release threshold is unlimited: memory a call frees stays
+// reserved for the library's next calls, so a steady stream of calls maps
+// no new memory (the device's default pool would hand freed memory back at
+// every synchronisation).  The caller's own allocations are untouched.
+static cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s)
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static cudaMemPool_t pools[MAX_DEV] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!pools[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t np = nullptr;
+            e = cudaMemPoolCreate(&np, &props);
+            if (e != cudaSuccess) return e;
+            uint64_t keep = UINT64_MAX;
+            e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep);
+            if (e != cudaSuccess) {
+                cudaMemPoolDestroy(np);
+                return e;
+            }
+            pools[dev] = np;
+        }
+        pool = pools[dev];
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
 static size_t esize(lizard_dtype dt) { return dt == LIZARD_F32 ? 4 : 2; }
 static bool dtype_ok(lizard_dtype dt) { return dt == LIZARD_F32 || dt == LIZARD_BF16; }
 
@@ -191,7 +230,7 @@ static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensor
 // (batch, head) units and a long prompt the sequence is split into segments
 // that run side by side, after a pre-pass that computes every segment's
 // start state; `scratch` (nullable) holds those states, else they live in
-// stream-ordered temporary memory (cudaMallocAsync / cudaFreeAsync on `s`).
+// stream-ordered scratch from the library's pool (freed on `s`).
 static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, float *scratch = nullptr,
                                        size_t scratch_bytes = 0, int force_segments = 0)
 {
@@ -213,7 +252,7 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
         if (scratch) {
             if (scratch_bytes < need) return LIZARD_ERR_UNSUPPORTED;
             seg_states = scratch;
-        } else if (cudaMallocAsync(reinterpret_cast<void **>(&seg_states), need, s) == cudaSuccess) {
+        } else if (scratch_alloc(reinterpret_cast<void **>(&seg_states), need, s) == cudaSuccess) {
             owned = true;
         } else {
             cudaGetLastError();
@@ -278,7 +317,7 @@ static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
 }
 
 // Gradients: the two-sweep kernel over every unit, then the reduction of the
-// per-unit d mu and d alpha parts.  Scratch in stream-ordered memory.
+// per-unit d mu and d alpha parts.  Scratch from the library's pool.
 template <typename T, int D>
 static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha, cudaStream_t s)
 {
@@ -288,7 +327,7 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
     const size_t dmu_bytes = units * ba.m * D * sizeof(float);
     const size_t bytes = xq_bytes + 2 * row_bytes + dmu_bytes + units * sizeof(float);
     uint8_t *scratch = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), bytes, s) != cudaSuccess) {
+    if (scratch_alloc(reinterpret_cast<void **>(&scratch), bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return LIZARD_ERR_CUDA;
     }
@@ -327,7 +366,7 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     const size_t xq_bytes = (size_t)units * L * D * sizeof(float);
     const size_t row_bytes = ((size_t)units * L * sizeof(float) + 255) & ~(size_t)255;
     uint8_t *scratch = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes, s) != cudaSuccess) {
+    if (scratch_alloc(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return LIZARD_ERR_CUDA;
     }

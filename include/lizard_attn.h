@@ -32,6 +32,12 @@
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and touches no buffer.
  *   - Errors are returned as lizard_status.  Nothing aborts, throws or traps.
+ *   - Scratch: a call that needs temporary device memory (a prompt run as
+ *     sequence segments, the backward pass) takes it stream-ordered on
+ *     `stream` from a memory pool the library owns (one per device) and
+ *     frees it there.  Freed memory stays reserved in that pool for the
+ *     library's later calls until the process exits; failure to allocate
+ *     is LIZARD_ERR_CUDA (a prefill then runs unsegmented instead).
  *   - Supported shapes: d_k == d_v in {64, 128}; 1 <= w <= LIZARD_MAX_WINDOW;
  *     0 <= m <= LIZARD_MAX_META.  Anything else in range but not built is
  *     LIZARD_ERR_UNSUPPORTED; anything meaningless is LIZARD_ERR_INVALID_ARG.
@@ -138,7 +144,7 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
  * Like lizard_attn_prefill it allocates only when a prompt runs as sequence
  * segments (few batch x head units, long L): then the segments' start
  * states and a copy of the first segment's S and window history live in
- * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * the library's scratch (see the conventions above).
  * L == 0 or B == 0 is a no-op.  Precondition: 0 <= pos[b] < 2^40 (a state
  * written by this library always is).  While the call runs, pos[b] carries
  * an arrival count in its high bits; it holds p + L again once the work is
@@ -197,8 +203,10 @@ LIZARD_API lizard_status lizard_attn_prefill_noalloc(const void *q, const void *
  *                                   aligned
  * Gradients are computed in fp32 from the stored input bits (every gate
  * value is handled: all exponents the kernel takes are <= 0) and rounded
- * to dtype once.  The call allocates its scratch on `stream` (cudaMallocAsync
- * / cudaFreeAsync): 4 (L dk + 2 L + m dk + 1) bytes per (batch, head) unit.
+ * to dtype once.  Scratch (see the conventions above) per (batch, head)
+ * unit: for bf16 with dk == 128 and w <= 65 (tensor cores) the bf16 state
+ * and state gradient at every 64-token chunk boundary plus 4 (L dk + 2 L)
+ * bytes, otherwise 4 (L dk + 2 L + m dk + 1) bytes.
  * L == 0 or B == 0 writes zero dmeta_k and dalpha and nothing else.
  */
 LIZARD_API lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, const void *g,
