@@ -8,7 +8,9 @@ d128 bf16, w64, m4 meta keys, alpha 1): gate log-sigmoid and log-space
 cumulative decay, intra- and inter-chunk gated linear attention, window +
 meta-sink softmax, alpha combine and the state hand-off, all in the library's
 kernels.  The decode step (64 sequences x H32, d128, w64, m4, fp32 state) is
-timed in the same run and reported under "decode".  Inputs are seeded
+timed in the same run and reported under "decode", and the backward pass of
+the same prefill (dq, dk, dv, dg, d meta, d alpha for a seeded upstream
+gradient: the training step of the operator) under "backward".  Inputs are seeded
 synthetic tensors (no dataset, no weights) larger than L2 and resident in HBM
 before the timed region.
 
@@ -57,6 +59,14 @@ def prefill_bytes(wl, B=None) -> int:
     es = 2 if wl.dtype == "bf16" else 4
     units = B * wl.H
     return units * (wl.L * 5 * wl.dk * es + wl.dk * wl.dv * 4 + 2 * wl.w * wl.dk * es)
+
+
+def backward_bytes(wl, B=None) -> int:
+    """q, k, v, g and the upstream gradient dy read, dq, dk, dv, dg written
+    once (9 d elements per token and head)."""
+    B = wl.B if B is None else B
+    es = 2 if wl.dtype == "bf16" else 4
+    return B * wl.H * wl.L * 9 * wl.dk * es
 
 
 def prefill_flops(wl, B=None) -> int:
@@ -271,7 +281,7 @@ def per_launch_ms(fn, steps, stream):
 def run_ours(args, world, rank, local):
     from hybrid_gated_linear_attn_b300 import LizardState, lizard_attn_decode_step, lizard_attn_prefill
     from hybrid_gated_linear_attn_b300 import lizard_attn as LA
-    from hybrid_gated_linear_attn_b300 import lizard_check_device_status
+    from hybrid_gated_linear_attn_b300 import lizard_attn_backward, lizard_check_device_status
 
     torch.cuda.set_device(local)
     LA.library()  # fails loudly if the CUDA library is missing
@@ -327,6 +337,16 @@ def run_ours(args, world, rank, local):
         dms = time_loop(dstep, dsteps, max(args.warmup, 3), stream)
         dms = max_over_ranks(dms, world)
         dlaunch_ms = dms  # one kernel per decode step: the timed average is its duration
+
+        # ---- backward of the prefill (training), same run ----
+        gen = torch.Generator().manual_seed(rank_seed(wl.seed + 11, rank))
+        dy_b = torch.randn(q.shape, generator=gen).to(q.dtype).cuda()
+
+        def bstep():
+            lizard_attn_backward(q, k, v, g, mu, wl.alpha, wl.w, dy_b, stream=stream)
+
+        bsteps = max(3, min(args.steps, 10))
+        bms = max_over_ranks(time_loop(bstep, bsteps, max(args.warmup, 2), stream), world)
     lizard_check_device_status(stream)
     clock = clocks.summary()
 
@@ -358,6 +378,8 @@ def run_ours(args, world, rank, local):
     achieved_tfs = nflops / (launch_ms * 1e-3) / 1e12
     d_nbytes = decode_bytes(dwl)
     d_gbs = d_nbytes / (dlaunch_ms * 1e-3) / 1e9
+    b_nbytes = backward_bytes(wl)
+    b_gbs = b_nbytes / (bms * 1e-3) / 1e9
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -379,6 +401,14 @@ def run_ours(args, world, rank, local):
                                 "frac": d_gbs / peaks["hbm_gbs"], "peak_source": peak_src,
                                 "traffic": ncu_traffic("decode", DECODE_KERNEL_SRC),
                                 "launch_ms": dlaunch_ms, "algorithmic_bytes": d_nbytes}},
+        "backward": {"value": world * tokens_rank / (bms * 1e-3), "unit": "tokens/s", "ms_per_step": bms,
+                     "steps": bsteps,
+                     "train_value": world * tokens_rank / ((ms + bms) * 1e-3),
+                     "train_unit": "tokens/s (prefill + backward)",
+                     "roofline": {"bound": "hbm", "achieved": b_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": b_gbs / peaks["hbm_gbs"], "peak_source": peak_src, "traffic": None,
+                                  "kernel": "backward call (chunk states, query side, key side)",
+                                  "launch_ms": bms, "algorithmic_bytes": b_nbytes}},
         "e2e": {"value": world * tokens_rank / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * 1,
@@ -401,7 +431,7 @@ def run_profile_case(args):
     the program that ncu captures on a small case.  ``--batch`` overrides the
     workload's batch (sequences)."""
     from hybrid_gated_linear_attn_b300 import LizardState, lizard_attn_decode_step, lizard_attn_prefill
-    from hybrid_gated_linear_attn_b300 import lizard_check_device_status
+    from hybrid_gated_linear_attn_b300 import lizard_attn_backward, lizard_check_device_status
 
     wl = WORKLOADS[args.workload]
     if args.batch:
@@ -414,6 +444,11 @@ def run_profile_case(args):
         y = torch.empty_like(v)
         st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
         fn = lambda: lizard_attn_prefill(q, k, v, g, mu, wl.alpha, wl.w, y=y, state=st)  # noqa: E731
+    elif args.profile_case == "backward":
+        inp = prefill_inputs(wl)
+        q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
+        dy = torch.randn(q.shape, generator=torch.Generator().manual_seed(wl.seed + 11)).to(q.dtype).cuda()
+        fn = lambda: lizard_attn_backward(q, k, v, g, mu, wl.alpha, wl.w, dy)  # noqa: E731
     else:
         init = decode_initial_state(wl)
         st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=torch_dtype(wl.dtype))
@@ -438,7 +473,7 @@ def main(argv=None):
     ap.add_argument("--sample-heads", type=int, default=None,
                     help="(batch, head) units in the oracle's timed sample (default: the whole workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "backward"], default=None,
                     help="only launch this operator W + K times (a small program for ncu); no JSON line")
     ap.add_argument("--workload", default=None, help="workload of --profile-case (default: the bench's)")
     ap.add_argument("--batch", type=int, default=0, help="batch override for --profile-case")
@@ -447,7 +482,7 @@ def main(argv=None):
     world, rank, local = dist_setup()
     if args.profile_case:
         if args.workload is None:
-            args.workload = "llama3_8b" if args.profile_case == "prefill" else "decode"
+            args.workload = "decode" if args.profile_case == "decode" else "llama3_8b"
         return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)

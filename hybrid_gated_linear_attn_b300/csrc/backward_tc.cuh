@@ -78,6 +78,23 @@ __device__ __forceinline__ void local_prefix(const uint8_t *gtile, int p, int hq
     tot[hq * 128 + 2 * p] = run.x;
     tot[hq * 128 + 2 * p + 1] = run.y;
 }
+// The same from gate logits held in registers (bf16 pairs of dims 2p, 2p+1).
+__device__ __forceinline__ void local_prefix_regs(const uint32_t (&gr)[16], int p, int hq, int n, Prefix &pf,
+                                                  float *tot)
+{
+    float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+        const float2 g = bf2_to_f2(gr[tt]);
+        if (16 * hq + tt < n) {
+            run.x += log2_sigmoid(g.x);
+            run.y += log2_sigmoid(g.y);
+        }
+        pf.b[tt] = run;
+    }
+    tot[hq * 128 + 2 * p] = run.x;
+    tot[hq * 128 + 2 * p + 1] = run.y;
+}
 // Adds the earlier quarters' totals; returns b_last (the chunk total).
 __device__ __forceinline__ float2 finish_prefix(int p, int hq, Prefix &pf, const float *tot)
 {
@@ -102,13 +119,15 @@ __device__ __forceinline__ float2 finish_prefix(int p, int hq, Prefix &pf, const
 
 // ============================================================ chunk states
 struct StatesArgs {
-    __nv_bfloat16 *Sb;  // [units][nchunks][D][D]  state before chunk c
-    __nv_bfloat16 *Ha;  // [units][nchunks][D][D]  dLoss/d(state after chunk c)
+    __nv_bfloat16 *Sb;       // [units][nchunks][D][D]  state before chunk c
+    __nv_bfloat16 *Ha;       // [units][nchunks][D][D]  dLoss/d(state after chunk c)
+    const __nv_bfloat16 *g;  // [units][L][D] gate logits (read into registers a chunk ahead)
     int L, nchunks;
 };
 
-// Shared memory: two stages of (g, x, y) tiles, two operand tiles, vectors.
-constexpr uint32_t ST_STAGE = 3 * 2 * TILE;                 // g | x | y, 16 KB each
+// Shared memory (about 100 KB, two CTAs per SM): two stages of (x, y)
+// tiles, two operand tiles, vectors.
+constexpr uint32_t ST_STAGE = 2 * 2 * TILE;                 // x | y, 16 KB each
 constexpr uint32_t ST_OP = 2 * ST_STAGE;                    // operand tiles [2] (16 KB each)
 constexpr uint32_t ST_VEC = ST_OP + 2 * 2 * TILE;           // dec[128], tot[4][128]
 constexpr uint32_t ST_BAR = ST_VEC + (128 + 512) * 4;       // bars: tma[2], mma
@@ -120,7 +139,7 @@ constexpr uint32_t ST_SMEM = ST_TSLOT + 8 + 1024;
 // transposed in tensor memory (lane = value dim j, column = key dim i):
 //   store X (row i = key dim) to out[c]; X^T <- X^T diag(2^{b_last}) + y^T O,
 //   O = k 2^{b_last - b} (forward) or q 2^{b} (backward).
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     chunk_states_kernel(const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq,
                         const __grid_constant__ CUtensorMap tdy, const StatesArgs a)
@@ -164,30 +183,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto issue = [&](int idx) {
         const int c = chunk_of(idx), s = idx & 1;
         uint8_t *st = sm + s * ST_STAGE;
-        mbar_arrive_expect_tx(&bar_tma[s], 3 * 2 * TILE);
-        tma_load_3d(st, &tg, &bar_tma[s], 0, c * C, unit);
-        tma_load_3d(st + TILE, &tg, &bar_tma[s], 64, c * C, unit);
-        tma_load_3d(st + 2 * TILE, mx, &bar_tma[s], 0, c * C, unit);
-        tma_load_3d(st + 3 * TILE, mx, &bar_tma[s], 64, c * C, unit);
-        tma_load_3d(st + 4 * TILE, my, &bar_tma[s], 0, c * C, unit);
-        tma_load_3d(st + 5 * TILE, my, &bar_tma[s], 64, c * C, unit);
+        mbar_arrive_expect_tx(&bar_tma[s], 2 * 2 * TILE);
+        tma_load_3d(st, mx, &bar_tma[s], 0, c * C, unit);
+        tma_load_3d(st + TILE, mx, &bar_tma[s], 64, c * C, unit);
+        tma_load_3d(st + 2 * TILE, my, &bar_tma[s], 0, c * C, unit);
+        tma_load_3d(st + 3 * TILE, my, &bar_tma[s], 64, c * C, unit);
     };
     if (tid == 0) issue(0);
     uint32_t tma_use[2] = {0, 0}, mma_use = 0, mma_issued = 0, tma_issued[2] = {1, 0};
     bool ok = true;
     const int p = tid & 63, hq = tid >> 6;
     const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
+    // gate logits of dims 2p, 2p+1 for this thread's 16 tokens, one chunk ahead
+    const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * D) + p;
+    uint32_t gnext[16];
+    auto load_g = [&](int idx) {
+        const int c = chunk_of(idx);
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+            const int row = c * C + 16 * hq + tt;
+            gnext[tt] = row < L ? gp[(size_t)row * (D / 2)] : 0u;
+        }
+    };
+    load_g(0);
 
     for (int idx = 0; idx < nch && ok; ++idx) {
         const int c = chunk_of(idx), s = idx & 1;
         const int n = min(C, L - c * C);
         uint8_t *st = sm + s * ST_STAGE;
+        uint32_t gcur[16];
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) gcur[tt] = gnext[tt];
+        if (idx + 1 < nch) load_g(idx + 1);
         ok = cta_wait(&bar_tma[s], tma_use[s]);
         if (!ok) break;
         ++tma_use[s];
         // gate prefix and the operand tile O[s]
         Prefix pf;
-        local_prefix(st, p, hq, n, pf, tot);
+        local_prefix_regs(gcur, p, hq, n, pf, tot);
         __syncthreads();
         const float2 bl = finish_prefix(p, hq, pf, tot);
         if (hq == 0) {
@@ -201,7 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int tt = 0; tt < 16; ++tt) {
                 const int t = 16 * hq + tt;
                 const uint32_t o = kblk + sw128_offset(t, kbyte);
-                const float2 x = bf2_to_f2(*reinterpret_cast<const uint32_t *>(st + 2 * TILE + o));
+                const float2 x = bf2_to_f2(*reinterpret_cast<const uint32_t *>(st + o));
                 const float2 e = rev ? make_float2(ex2(pf.b[tt].x), ex2(pf.b[tt].y))
                                      : make_float2(ex2(bl.x - pf.b[tt].x), ex2(bl.y - pf.b[tt].y));
                 *reinterpret_cast<uint32_t *>(op + o) = f2_to_bf2(x.x * e.x, x.y * e.y);
@@ -242,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            const uint32_t yb = sb + s * ST_STAGE + 4 * TILE, ob = sb + ST_OP + s * 2 * TILE;
+            const uint32_t yb = sb + s * ST_STAGE + 2 * TILE, ob = sb + ST_OP + s * 2 * TILE;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem, smem_desc(yb + kk * 2048, TILE, 1024), smem_desc(ob + kk * 2048, TILE, 1024),
@@ -1067,9 +1100,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<uint4 *>(sm + KO_AT + sw128_offset(t, s0 * 2 + 16)) =
                         make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
-            } else {
+            }
+            {
                 // KL into the KR slot (KR was read by M1b, which is done)
-                for (int e = tid - 128; e < C * 64; e += 128) {
+                for (int e = tid; e < C * 64; e += THREADS) {
                     const int s2 = e / 64, ip = e % 64, i = 2 * ip;
                     const uint32_t o = (i / 64) * TILE + sw128_offset(s2, (i % 64) * 2);
                     const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + KO_K + o));
@@ -1195,26 +1229,43 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) bk[t * D + 64 * colh + 32 * jj + 16 * hs + e] = term[jj][e];
         }
-        __syncthreads();
-        // ---- dg = dlog gamma * sigmoid(-g)
-        if (tid < D) {
-            const int i = tid;
+        // ---- dg = dlog gamma * sigmoid(-g).  sigmoid(-g) = 2^{log2 sigmoid(-g)}
+        // for every element first (into the state-gradient slot: its readers
+        // are done), then two threads per column scan half a chunk each.
+        __syncthreads();  // the terms and k dk_inter of every row are written
+        float *sg = reinterpret_cast<float *>(sm + KO_H);
+        for (int e = tid; e < C * 64; e += THREADS) {
+            const int t2 = e / 64, ip = e % 64, i = 2 * ip;
+            const float2 gv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(
+                sm + KO_G + (i / 64) * TILE + sw128_offset(t2, (i % 64) * 2)));
+            sg[t2 * D + i] = ex2(log2_sigmoid(-gv.x));
+            sg[t2 * D + i + 1] = ex2(log2_sigmoid(-gv.y));
+        }
+        float *part = Ep;  // [2][128]: the upper half's sum of terms, the lower half's sum of k dk_inter
+        const int i = tid & 127, half = tid >> 7;
+        const int h0 = half * (C / 2), h1 = min(n, h0 + C / 2);
+        {
+            float sr = 0.f, sf = 0.f;
+            for (int t2 = h0; t2 < h1; ++t2) {
+                sr += bk[t2 * D + i];
+                sf += yo[t2 * D + i];
+            }
+            __syncthreads();  // Ep (the E parts) is read below, before it is reused
             const float E = (Ep[i] + Ep[128 + i]) * ex2(blv[i]);
-            // forward exclusive prefix of k * dk_inter, in place
-            float f = 0.f;
-            for (int t2 = 0; t2 < n; ++t2) {
+            __syncthreads();
+            if (half == 1) part[i] = sr;        // terms of rows 32 .. 63, for the reverse prefix of rows < 32
+            if (half == 0) part[128 + i] = sf;  // k dk_inter of rows 0 .. 31, for the forward prefix of rows >= 32
+            __syncthreads();
+            float run = (half == 0 ? part[i] : 0.f) + E;  // reverse: later rows first
+            float f = half == 1 ? part[128 + i] : 0.f;   // forward exclusive prefix
+            for (int t2 = h0; t2 < h1; ++t2) {  // forward prefix of k dk_inter, in place
                 const float x = yo[t2 * D + i];
                 yo[t2 * D + i] = f;
                 f += x;
             }
-            float run = 0.f;
-            for (int t2 = n - 1; t2 >= 0; --t2) {
+            for (int t2 = h1 - 1; t2 >= h0; --t2) {
                 run += bk[t2 * D + i];
-                const float gv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                    sm + KO_G + (i / 64) * TILE + sw128_offset(t2, (i % 64) * 2)));
-                // sigmoid(-g) = 2^{log2 sigmoid(-g)}
-                a.dg[((size_t)unit * L + c0 + t2) * D + i] =
-                    __float2bfloat16_rn((run + E + yo[t2 * D + i]) * ex2(log2_sigmoid(-gv)));
+                a.dg[((size_t)unit * L + c0 + t2) * D + i] = __float2bfloat16_rn((run + yo[t2 * D + i]) * sg[t2 * D + i]);
             }
         }
     } while (false);

@@ -386,7 +386,7 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     if (rc == LIZARD_OK && dmu && cudaMemsetAsync(dmu, 0, sizeof(float) * ba.H * ba.m * D, s) != cudaSuccess)
         rc = LIZARD_ERR_CUDA;
     if (rc == LIZARD_OK) {
-        bwdtc::StatesArgs sa{Sb, Ha, L, nch};
+        bwdtc::StatesArgs sa{Sb, Ha, static_cast<const __nv_bfloat16 *>(ba.g), L, nch};
         if (cudaFuncSetAttribute(bwdtc::chunk_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::ST_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
