@@ -146,3 +146,12 @@ def rel_l2(x: torch.Tensor, ref: torch.Tensor) -> float:
     x = x.double()
     ref = ref.double()
     return float(torch.linalg.vector_norm(x - ref) / torch.linalg.vector_norm(ref))
+
+
+def gate_projection_inputs(B: int, L: int, dmodel: int, H: int, dk: int, seed: int = 5) -> dict:
+    """Layer input x [B, L, dmodel] ~ N(0, 1) and gate weight W [H dk, dmodel]
+    ~ N(0, 1) / sqrt(dmodel) (so the logits are ~N(0, 1)), both bf16."""
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, L, dmodel, generator=gen).to(torch.bfloat16)
+    W = (torch.randn(H * dk, dmodel, generator=gen) / math.sqrt(dmodel)).to(torch.bfloat16)
+    return {"x": x, "W": W}

@@ -256,3 +256,19 @@ def gla_product_form(q, k, v, g, S0=None, *, lib=None):
 def log_sigmoid(x: float, *, lib=None) -> float:
     lib = lib or load()
     return lib.oracle_log_sigmoid(float(x))
+
+
+def gate_projection(x, W, H):
+    """Gate logits of the gated linear attention from the layer input: the
+    gate module Gamma = sigmoid(W_gamma x) of Lizard (gist.science/de
+    section 2 item 1) feeds the operator its logits g = W_gamma x.
+
+    x [B, L, dmodel], W [H * dk, dmodel] (a linear layer's weight), both
+    widened exactly to fp64; returns g [B, H, L, dk] fp64 (head-major, the
+    operator's layout): g[b, h, t, i] = sum_c x[b, t, c] W[h dk + i, c].
+    """
+    B, L, dm = x.shape
+    N = W.shape[0]
+    dk = N // H
+    g = x.double().reshape(B * L, dm) @ W.double().t()
+    return g.reshape(B, L, H, dk).permute(0, 2, 1, 3).contiguous()

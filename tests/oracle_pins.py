@@ -341,6 +341,27 @@ def pin_backward_open_gates_have_no_gate_gradient(lib):
     assert float(got["dq"].abs().max()) > 0.0
 
 
+# --- gate projection -----------------------------------------------------------
+
+def pin_gate_projection_brute_force(lib):
+    # Every output element by an explicit sum over the model dimension, with
+    # the head-major placement g[b, h, t, i] <- row h * dk + i of W.
+    B, L, dm, H, dk = 2, 3, 5, 2, 3
+    gen = _gen(131)
+    x = torch.randn(B, L, dm, generator=gen).to(torch.bfloat16)
+    W = torch.randn(H * dk, dm, generator=gen).to(torch.bfloat16)
+    got = O.gate_projection(x, W, H)
+    assert tuple(got.shape) == (B, H, L, dk)
+    for b in range(B):
+        for h in range(H):
+            for t in range(L):
+                for i in range(dk):
+                    ref = 0.0
+                    for c in range(dm):
+                        ref += float(x[b, t, c]) * float(W[h * dk + i, c])
+                    assert abs(float(got[b, h, t, i]) - ref) <= 1e-12 * max(1.0, abs(ref)), (b, h, t, i)
+
+
 PINS = [
     pin_log_sigmoid_vs_scipy,
     pin_recurrence_equals_product_form,
@@ -357,4 +378,5 @@ PINS = [
     pin_backward_vs_finite_differences,
     pin_backward_vs_autograd,
     pin_backward_open_gates_have_no_gate_gradient,
+    pin_gate_projection_brute_force,
 ]
