@@ -281,7 +281,8 @@ def per_launch_ms(fn, steps, stream):
 def run_ours(args, world, rank, local):
     from hybrid_gated_linear_attn_b300 import LizardState, lizard_attn_decode_step, lizard_attn_prefill
     from hybrid_gated_linear_attn_b300 import lizard_attn as LA
-    from hybrid_gated_linear_attn_b300 import lizard_attn_backward, lizard_check_device_status
+    from hybrid_gated_linear_attn_b300 import lizard_attn_backward, lizard_check_device_status, lizard_gate_projection
+    from hybrid_gated_linear_attn_b300.inputs import gate_projection_inputs
 
     torch.cuda.set_device(local)
     LA.library()  # fails loudly if the CUDA library is missing
@@ -347,6 +348,19 @@ def run_ours(args, world, rank, local):
 
         bsteps = max(3, min(args.steps, 10))
         bms = max_over_ranks(time_loop(bstep, bsteps, max(args.warmup, 2), stream), world)
+
+        # ---- gate projection of the same layer (x [B, L, 4096] -> g), same run ----
+        dmodel = 4096
+        proj = gate_projection_inputs(Bl, wl.L, dmodel, wl.H, wl.dk, seed=rank_seed(wl.seed + 23, rank))
+        px, pw = proj["x"].cuda(), proj["W"].cuda()
+        pg = torch.empty(Bl, wl.H, wl.L, wl.dk, dtype=torch.bfloat16, device="cuda")
+
+        def pstep():
+            lizard_gate_projection(px, pw, wl.H, g=pg, stream=stream)
+
+        psteps = max(3, min(args.steps, 10))
+        pms = max_over_ranks(time_loop(pstep, psteps, max(args.warmup, 2), stream), world)
+        pflops = 2.0 * Bl * wl.L * wl.H * wl.dk * dmodel
     lizard_check_device_status(stream)
     clock = clocks.summary()
 
@@ -409,6 +423,13 @@ def run_ours(args, world, rank, local):
                                   "frac": b_gbs / peaks["hbm_gbs"], "peak_source": peak_src, "traffic": None,
                                   "kernel": "backward call (chunk states, query side, key side)",
                                   "launch_ms": bms, "algorithmic_bytes": b_nbytes}},
+        "gate_projection": {"value": world * tokens_rank / (pms * 1e-3), "unit": "tokens/s", "ms_per_step": pms,
+                            "steps": psteps, "shape": f"x [{Bl}, {wl.L}, {dmodel}] x W^T [{dmodel}, {wl.H * wl.dk}]",
+                            "roofline": {"bound": "tensor", "achieved": pflops / (pms * 1e-3) / 1e12,
+                                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                         "frac": pflops / (pms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                         "peak_source": peak_src, "traffic": None, "kernel": "gate_proj_kernel",
+                                         "launch_ms": pms, "algorithmic_flops": pflops}},
         "e2e": {"value": world * tokens_rank / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * 1,

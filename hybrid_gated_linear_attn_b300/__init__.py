@@ -11,6 +11,7 @@ from .lizard_attn import (  # noqa: F401
     lizard_attn_prefill_continue,
     lizard_attn_prefill_noalloc,
     lizard_check_device_status,
+    lizard_gate_projection,
     lizard_state_init,
     lizard_status_string,
 )

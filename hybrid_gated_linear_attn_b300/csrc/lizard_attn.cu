@@ -5,7 +5,8 @@
 // the segment pre-pass of prefill_state.cuh), prefill_tc.cuh (bf16, d = 128,
 // w > 65: tensor cores), prefill_simt.cuh (fp32 and d = 64: CUDA cores, exact
 // fp32), prefill_cont.cuh (start position of a continued prompt),
-// backward_simt.cuh (gradients) and the state initialiser below.  Declarations and the contract of every entry point are
+// backward_simt.cuh / backward_tc.cuh (gradients), gate_proj.cuh (the gate
+// projection) and the state initialiser below.  Declarations and the contract of every entry point are
 // in include/lizard_attn.h.
 #include <cuda_runtime.h>
 
@@ -24,6 +25,7 @@
 #include "prefill_cont.cuh"
 #include "backward_simt.cuh"
 #include "backward_tc.cuh"
+#include "gate_proj.cuh"
 
 namespace lizard {
 
@@ -422,6 +424,21 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     return rc;
 }
 
+// [rows][K] bf16 row-major as a 3-D tensor {K, rows, 1}; 64 x 128 boxes,
+// 128B swizzle, rows and columns past the end read as zero.
+static bool make_rows_map(CUtensorMap *map, const void *base, int rows, int K)
+{
+    encode_tiled_fn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)rows * K * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- allocation-free prefill
 // Segment states of lizard_attn_prefill_noalloc: a fixed array in device
 // memory, held by every GPU that loads this library until the process ends.
@@ -605,6 +622,30 @@ lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, 
         return dk == 128 ? launch_backward<__nv_bfloat16, 128>(ba, dmu, dalpha, s)
                          : launch_backward<__nv_bfloat16, 64>(ba, dmu, dalpha, s);
     return dk == 128 ? launch_backward<float, 128>(ba, dmu, dalpha, s) : launch_backward<float, 64>(ba, dmu, dalpha, s);
+}
+
+lizard_status lizard_gate_projection(const void *x, const void *w_gamma, int B, int L, int dmodel, int H, int dk,
+                                    lizard_dtype dtype, void *g, lizard_stream_t stream)
+{
+    if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
+    if (B < 0 || L < 0 || dmodel < 1 || H < 1 || dk < 1) return LIZARD_ERR_INVALID_ARG;
+    const int64_t M = (int64_t)B * L;
+    if (M > 0 && (!x || !w_gamma || !g)) return LIZARD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gamma) || !aligned16(g)) return LIZARD_ERR_INVALID_ARG;
+    if (dtype != LIZARD_BF16 || dk != gproj::BN || dmodel % 8 != 0) return LIZARD_ERR_UNSUPPORTED;
+    if (M > 2147483647LL || (int64_t)H * dk > 2147483647LL || M * dmodel > ((int64_t)1 << 40))
+        return LIZARD_ERR_UNSUPPORTED;
+    if (M == 0) return LIZARD_OK;
+    CUtensorMap tx, tw;
+    if (!make_rows_map(&tx, x, (int)M, dmodel) || !make_rows_map(&tw, w_gamma, H * dk, dmodel)) return LIZARD_ERR_CUDA;
+    if (cudaFuncSetAttribute(gproj::gate_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gproj::SMEM) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    const int64_t tiles = ((M + gproj::BM - 1) / gproj::BM) * H;
+    if (tiles > 2147483647LL) return LIZARD_ERR_UNSUPPORTED;
+    gproj::Args ga{static_cast<__nv_bfloat16 *>(g), (int)M, dmodel, L, H};
+    gproj::gate_proj_kernel<<<(unsigned)tiles, gproj::THREADS, gproj::SMEM, (cudaStream_t)stream>>>(tx, tw, ga);
+    return launch_status();
 }
 
 lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,

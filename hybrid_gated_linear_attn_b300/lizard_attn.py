@@ -24,7 +24,8 @@ LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
 EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
-           "lizard_attn_backward", "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string")
+           "lizard_attn_backward", "lizard_gate_projection", "lizard_attn_decode_step", "lizard_check_device_status",
+           "lizard_status_string")
 
 
 class LizardError(RuntimeError):
@@ -65,6 +66,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lizard_attn_prefill_noalloc.restype = I
         lib.lizard_attn_backward.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
         lib.lizard_attn_backward.restype = I
+        lib.lizard_gate_projection.argtypes = [P, P, I, I, I, I, I, I, P, P]
+        lib.lizard_gate_projection.restype = I
         lib.lizard_attn_decode_step.argtypes = [P, P, P, P, P, F, I, P, SP, P]
         lib.lizard_attn_decode_step.restype = I
         lib.lizard_check_device_status.argtypes = [P]
@@ -202,6 +205,19 @@ def lizard_attn_backward(q, k, v, g, meta_k, alpha, w, dy, stream=None):
         _ptr(dmeta) if m > 0 else None, _ptr(dalpha), _stream(stream))
     _check(rc, "lizard_attn_backward")
     return dq, dk_, dv_, dg, dmeta, dalpha
+
+
+def lizard_gate_projection(x, w_gamma, H, g=None, stream=None) -> torch.Tensor:
+    """Gate logits g [B, H, L, dk] (head-major) = x [B, L, dmodel] times the
+    gate weight w_gamma [H * dk, dmodel] transposed."""
+    B, L, dmodel = x.shape
+    dk = w_gamma.shape[0] // H
+    if g is None:
+        g = torch.empty(B, H, L, dk, dtype=x.dtype, device=x.device)
+    rc = library().lizard_gate_projection(_ptr(x), _ptr(w_gamma), B, L, dmodel, H, dk, _dtype_code(x), _ptr(g),
+                                          _stream(stream))
+    _check(rc, "lizard_gate_projection")
+    return g
 
 
 def lizard_attn_decode_step(q, k, v, g, meta_k, alpha, state: LizardState, y=None, stream=None) -> torch.Tensor:

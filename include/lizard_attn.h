@@ -216,6 +216,23 @@ LIZARD_API lizard_status lizard_attn_backward(const void *q, const void *k, cons
                                    lizard_stream_t stream);
 
 /*
+ * lizard_gate_projection: the gate logits the operator takes, from the layer
+ * input -- the gate module Gamma = sigmoid(W_gamma x) of gist.science/de
+ * section 2 item 1 sits directly ahead of the operator; this computes its
+ * logits g = W_gamma x and writes them in the operator's head-major layout
+ * (the operator applies the log-sigmoid itself):
+ *   x        [B][L][dmodel]   bf16   layer input, row-major
+ *   w_gamma  [H * dk][dmodel] bf16   gate weight (a linear layer's weight)
+ *   g        [B][H][L][dk]    bf16   written: g[b][h][t][i] =
+ *                                    sum_c x[b][t][c] w_gamma[h dk + i][c]
+ * fp32 accumulation on the tensor cores, rounded to bf16 once.  Supported:
+ * bf16, dk == 128, dmodel a multiple of 8 (LIZARD_ERR_UNSUPPORTED
+ * otherwise).  B * L == 0 is a no-op.
+ */
+LIZARD_API lizard_status lizard_gate_projection(const void *x, const void *w_gamma, int B, int L, int dmodel,
+                                     int H, int dk, lizard_dtype dtype, void *g, lizard_stream_t stream);
+
+/*
  * lizard_attn_decode_step: one new token for each of st->B sequences and
  * st->H heads, continuing from `st` (updated in place).
  *   q, k, g  [B][H][dk]  st->dtype;  v [B][H][dv];  meta_k [H][m][dk]

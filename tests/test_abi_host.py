@@ -133,7 +133,7 @@ def test_state_init_rejects(lib):
 def test_binding_names_match_the_c_abi():
     import hybrid_gated_linear_attn_b300 as pkg
     for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
-                 "lizard_attn_backward",
+                 "lizard_attn_backward", "lizard_gate_projection",
                  "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string"):
         assert callable(getattr(pkg, name))
 
@@ -178,3 +178,20 @@ def backward(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128,
 ])
 def test_backward_rejects(lib, kw, code):
     assert backward(lib, **kw) == code
+
+
+def gproj(lib, x=A, w=A, Bn=2, L=128, dm=256, H=4, dk=128, dtype=LA.LIZARD_BF16, g=A):
+    return lib.lizard_gate_projection(x, w, Bn, L, dm, H, dk, dtype, g, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), INVALID), (dict(w=None), INVALID), (dict(g=None), INVALID), (dict(x=MIS), INVALID),
+    (dict(dtype=9), INVALID), (dict(Bn=-1), INVALID), (dict(dm=0), INVALID), (dict(H=0), INVALID),
+    (dict(dk=64), UNSUPPORTED), (dict(dtype=LA.LIZARD_F32), UNSUPPORTED), (dict(dm=100), UNSUPPORTED),
+])
+def test_gate_projection_rejects(lib, kw, code):
+    assert gproj(lib, **kw) == code
+
+
+def test_gate_projection_empty_is_ok(lib):
+    assert gproj(lib, x=None, w=None, g=None, L=0) == OK
