@@ -6,9 +6,10 @@
 // decides how much of the past each key dimension keeps; the operator takes
 // its logits g = W_gamma x (and applies the log-sigmoid itself).
 //
-// One CTA per 128 x 128 output tile (128 tokens x one head of dk = 128),
-// consecutive CTAs sweeping the heads of one token block (the x block and
-// all of W stay in L2).  A four-stage TMA pipeline feeds 64-wide K slices
+// One CTA per 128 x (128 NH) output tile (128 tokens x NH heads of dk =
+// 128; NH = 2 when the head count is even, which cuts the operand bytes per
+// flop by a quarter), consecutive CTAs sweeping the heads of one token block
+// (the x block and all of W stay in L2).  A four-stage TMA pipeline feeds 64-wide K slices
 // (128B-swizzled, K-major) to one MMA-issuing thread; the fp32 accumulator
 // lives in tensor memory; four epilogue warps convert and store each
 // token's 128 outputs (256 contiguous bytes).  Every wait is bounded: a
@@ -23,17 +24,22 @@ namespace gproj {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int BM = 128, DK = 128, BK = 64;
 constexpr int STAGES = 4;
 constexpr int THREADS = 256;
-constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;  // 16 KB each
-constexpr uint32_t STAGE = A_BYTES + B_BYTES;
-constexpr uint32_t OFF_BAR = STAGES * STAGE;
-constexpr uint32_t SMEM = OFF_BAR + (2 * STAGES + 1) * 8 + 16 + 1024;
 constexpr uint32_t WAIT = 1u << 21;
+template <int NH>
+struct Cfg {
+    static constexpr int BN = DK * NH;
+    static constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+    static constexpr uint32_t OFF_BAR = STAGES * STAGE;
+    static constexpr uint32_t SMEM = OFF_BAR + (2 * STAGES + 1) * 8 + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
 
 struct Args {
-    __nv_bfloat16 *g;  // [B][H][L][BN]
+    __nv_bfloat16 *g;  // [B][H][L][DK]
     int M, K, L, H;    // M = B * L tokens, K = dmodel
 };
 
@@ -46,10 +52,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t use, volatile i
     return false;
 }
 
-// grid = ceil(M / BM) * H: tile = blockIdx.x, head = tile % H, token block = tile / H.
+// grid = ceil(M / BM) * (H / NH): tile = blockIdx.x, heads NH (tile % (H / NH))
+// .. + NH - 1, token block = tile / (H / NH).  tw's box is BN rows high.
+template <int NH>
 __global__ void __launch_bounds__(THREADS, 1)
     gate_proj_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, const Args a)
 {
+    using G = Cfg<NH>;
+    constexpr int BN = G::BN;
+    constexpr uint32_t A_BYTES = G::A_BYTES, STAGE = G::STAGE, OFF_BAR = G::OFF_BAR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -58,7 +69,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *abort_f = reinterpret_cast<volatile int *>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % a.H, m0 = (blockIdx.x / a.H) * BM, n0 = h * BN;
+    const int HT = a.H / NH;
+    const int h0 = (blockIdx.x % HT) * NH, m0 = (blockIdx.x / HT) * BM, n0 = h0 * DK;
     const int KT = (a.K + BK - 1) / BK;
 
     if (warp == 1) {
@@ -132,9 +144,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
             tc_fence_after();
             const int b = m / a.L, t = m % a.L;
-            uint4 *dst = reinterpret_cast<uint4 *>(a.g + (((size_t)b * a.H + h) * a.L + t) * BN);
 #pragma unroll 1
             for (int cc = 0; cc < BN; cc += 16) {
+                uint4 *dst = reinterpret_cast<uint4 *>(a.g + (((size_t)b * a.H + h0 + cc / DK) * a.L + t) * DK);
                 uint32_t r[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + cc, r);
                 tmem_wait_ld();
@@ -145,8 +157,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     pk[e / 2] = *reinterpret_cast<uint32_t *>(&v2);
                 }
                 if (m < a.M) {
-                    dst[cc / 8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[cc / 8 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    dst[(cc % DK) / 8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[(cc % DK) / 8 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
             }
         }

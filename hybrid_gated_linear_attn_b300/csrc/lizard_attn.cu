@@ -424,15 +424,15 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     return rc;
 }
 
-// [rows][K] bf16 row-major as a 3-D tensor {K, rows, 1}; 64 x 128 boxes,
-// 128B swizzle, rows and columns past the end read as zero.
-static bool make_rows_map(CUtensorMap *map, const void *base, int rows, int K)
+// [rows][K] bf16 row-major as a 3-D tensor {K, rows, 1}; 64 x box_rows
+// boxes, 128B swizzle, rows and columns past the end read as zero.
+static bool make_rows_map(CUtensorMap *map, const void *base, int rows, int K, int box_rows)
 {
     encode_tiled_fn enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, 1};
     cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)rows * K * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -632,19 +632,23 @@ lizard_status lizard_gate_projection(const void *x, const void *w_gamma, int B, 
     const int64_t M = (int64_t)B * L;
     if (M > 0 && (!x || !w_gamma || !g)) return LIZARD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w_gamma) || !aligned16(g)) return LIZARD_ERR_INVALID_ARG;
-    if (dtype != LIZARD_BF16 || dk != gproj::BN || dmodel % 8 != 0) return LIZARD_ERR_UNSUPPORTED;
+    if (dtype != LIZARD_BF16 || dk != gproj::DK || dmodel % 8 != 0) return LIZARD_ERR_UNSUPPORTED;
     if (M > 2147483647LL || (int64_t)H * dk > 2147483647LL || M * dmodel > ((int64_t)1 << 40))
         return LIZARD_ERR_UNSUPPORTED;
     if (M == 0) return LIZARD_OK;
+    // two heads per tile when the head count allows it
+    const int nh = H % 2 == 0 ? 2 : 1;
     CUtensorMap tx, tw;
-    if (!make_rows_map(&tx, x, (int)M, dmodel) || !make_rows_map(&tw, w_gamma, H * dk, dmodel)) return LIZARD_ERR_CUDA;
-    if (cudaFuncSetAttribute(gproj::gate_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gproj::SMEM) != cudaSuccess)
+    if (!make_rows_map(&tx, x, (int)M, dmodel, gproj::BM) || !make_rows_map(&tw, w_gamma, H * dk, dmodel, gproj::DK * nh))
         return LIZARD_ERR_CUDA;
-    const int64_t tiles = ((M + gproj::BM - 1) / gproj::BM) * H;
+    const int64_t tiles = ((M + gproj::BM - 1) / gproj::BM) * (H / nh);
     if (tiles > 2147483647LL) return LIZARD_ERR_UNSUPPORTED;
     gproj::Args ga{static_cast<__nv_bfloat16 *>(g), (int)M, dmodel, L, H};
-    gproj::gate_proj_kernel<<<(unsigned)tiles, gproj::THREADS, gproj::SMEM, (cudaStream_t)stream>>>(tx, tw, ga);
+    auto kern = nh == 2 ? gproj::gate_proj_kernel<2> : gproj::gate_proj_kernel<1>;
+    const uint32_t smem = nh == 2 ? gproj::Cfg<2>::SMEM : gproj::Cfg<1>::SMEM;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    kern<<<(unsigned)tiles, gproj::THREADS, smem, (cudaStream_t)stream>>>(tx, tw, ga);
     return launch_status();
 }
 
