@@ -46,6 +46,8 @@ struct BackwardArgs {
     float *lse, *drow;  // [units][L]     log-normaliser and D_t of each row
     float *dmu_part;    // [units][m][D]
     float *dalpha_part; // [units]
+    const float *alpha_h;  // per-head anchor weights (null: alpha)
+    int group;             // query heads per key/value head (k, v hold B x H / group heads)
 };
 
 constexpr int BW_C = 32;  // chunk length
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1) backward_simt_kernel(BackwardAr
     const int unit = blockIdx.x, h = unit % a.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = a.L, w = a.w, m = a.m;
-    const float alpha = a.alpha;
+    const float alpha = head_alpha(a.alpha_h, a.alpha, h);
 
     extern __shared__ float sm[];
     float *S = sm;                    // [D][LD] state (forward sweep) / state gradient (reverse sweep)
@@ -93,8 +95,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1) backward_simt_kernel(BackwardAr
 
     const size_t base = (size_t)unit * L * D;
     const T *q = static_cast<const T *>(a.q) + base;
-    const T *k = static_cast<const T *>(a.k) + base;
-    const T *v = static_cast<const T *>(a.v) + base;
+    const size_t kvbase = (size_t)kv_unit(unit, a.H, a.group) * L * D;
+    const T *k = static_cast<const T *>(a.k) + kvbase;
+    const T *v = static_cast<const T *>(a.v) + kvbase;
     const T *g = static_cast<const T *>(a.g) + base;
     const T *dy = static_cast<const T *>(a.dy) + base;
     const T *mu = static_cast<const T *>(a.mu) + (size_t)h * m * D;
@@ -398,9 +401,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1) backward_simt_kernel(BackwardAr
 }
 
 // d mu[h] = sum over the batch of the units' partials; d alpha = sum over all
-// units.  grid.x covers H * m * D elements; block 0 also sums d alpha.
+// units (per_head: d alpha[h] = sum over the batch, by block 0's first H
+// threads).  grid.x covers H * m * D elements; block 0 also sums d alpha.
 __global__ void backward_reduce_kernel(const float *dmu_part, const float *dalpha_part, int B, int H, int mD,
-                                       float *dmu, float *dalpha)
+                                       float *dmu, float *dalpha, int per_head)
 {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (dmu && e < H * mD) {
@@ -409,7 +413,13 @@ __global__ void backward_reduce_kernel(const float *dmu_part, const float *dalph
         for (int b = 0; b < B; ++b) s += dmu_part[((size_t)b * H + h) * mD + r];
         dmu[e] = s;
     }
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == 0 && per_head) {
+        for (int hh = threadIdx.x; hh < H; hh += blockDim.x) {
+            float s = 0.f;
+            for (int b = 0; b < B; ++b) s += dalpha_part[(size_t)b * H + hh];
+            dalpha[hh] = s;
+        }
+    } else if (blockIdx.x == 0) {
         __shared__ float red[256];
         float s = 0.f;
         for (long long u = threadIdx.x; u < (long long)B * H; u += blockDim.x) s += dalpha_part[u];
@@ -420,6 +430,24 @@ __global__ void backward_reduce_kernel(const float *dmu_part, const float *dalph
             __syncthreads();
         }
         if (threadIdx.x == 0) *dalpha = red[0];
+    }
+}
+
+// Grouped key/value heads: dk, dv of key/value head hk are the sums over
+// the group's query heads (the key and value feed every head of the group):
+// dst[b][hk][e] = sum_j src[b][hk group + j][e], in fp32, rounded once.
+// grid-stride over B * Hkv * LD elements (LD = L * D).
+template <typename T>
+__global__ void gqa_reduce_kernel(const T *src, T *dst, int B, int H, int group, long long LD)
+{
+    const int Hkv = H / group;
+    const long long n = (long long)B * Hkv * LD;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+        const long long r = e % LD, bh = e / LD;
+        const long long b = bh / Hkv, hk = bh % Hkv;
+        float s = 0.f;
+        for (int j = 0; j < group; ++j) s += to_f32(src[((b * H) + hk * group + j) * LD + r]);
+        dst[e] = from_f32<T>(s);
     }
 }
 

@@ -123,6 +123,7 @@ struct StatesArgs {
     __nv_bfloat16 *Ha;       // [units][nchunks][D][D]  dLoss/d(state after chunk c)
     const __nv_bfloat16 *g;  // [units][L][D] gate logits (read into registers a chunk ahead)
     int L, nchunks;
+    int H, group;            // query heads per key/value head (tk, tv map B x H / group heads)
 };
 
 // Shared memory (about 100 KB, two CTAs per SM): two stages of (x, y)
@@ -180,14 +181,15 @@ __global__ void __launch_bounds__(THREADS, 2)
         tmem_wait_st();
     }
     auto chunk_of = [&](int idx) { return rev ? nch - 1 - idx : idx; };
+    const int xyu = rev ? unit : kv_unit(unit, a.H, a.group);  // k, v come from the key/value head
     auto issue = [&](int idx) {
         const int c = chunk_of(idx), s = idx & 1;
         uint8_t *st = sm + s * ST_STAGE;
         mbar_arrive_expect_tx(&bar_tma[s], 2 * 2 * TILE);
-        tma_load_3d(st, mx, &bar_tma[s], 0, c * C, unit);
-        tma_load_3d(st + TILE, mx, &bar_tma[s], 64, c * C, unit);
-        tma_load_3d(st + 2 * TILE, my, &bar_tma[s], 0, c * C, unit);
-        tma_load_3d(st + 3 * TILE, my, &bar_tma[s], 64, c * C, unit);
+        tma_load_3d(st, mx, &bar_tma[s], 0, c * C, xyu);
+        tma_load_3d(st + TILE, mx, &bar_tma[s], 64, c * C, xyu);
+        tma_load_3d(st + 2 * TILE, my, &bar_tma[s], 0, c * C, xyu);
+        tma_load_3d(st + 3 * TILE, my, &bar_tma[s], 64, c * C, xyu);
     };
     if (tid == 0) issue(0);
     uint32_t tma_use[2] = {0, 0}, mma_use = 0, mma_issued = 0, tma_issued[2] = {1, 0};
@@ -305,9 +307,11 @@ struct QueryArgs {
     float *xq;                    // [units][L][D]  q * dq_gate
     float *lse2, *drow;           // [units][L]     base-2 log-normaliser, D_t
     float *dmu;                   // [H][m][D]      accumulated (zeroed by the host)
-    float *dalpha;                // accumulated (zeroed by the host)
+    float *dalpha;                // accumulated (zeroed by the host): [H] with alpha_h, else one value
     float alpha;
     int H, L, w, m, nchunks;
+    const float *alpha_h;         // per-head anchor weights (null: alpha)
+    int group;                    // query heads per key/value head
 };
 
 constexpr int META_ROWS = 16;
@@ -358,7 +362,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int L = a.L, w = a.w, m = a.m;
     const int c0 = c * C, n = min(C, L - c0);
     const bool has_prev = c > 0;
-    const float alpha = a.alpha;
+    const float alpha = head_alpha(a.alpha_h, a.alpha, h);
+    const int kvu = kv_unit(unit, a.H, a.group);
 
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -390,11 +395,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_3d(sm + QO_Q + hb * TILE, &tq, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + QO_DY + hb * TILE, &tdy, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + QO_G + hb * TILE, &tg, bar_in, 64 * hb, c0, unit);
-            tma_load_3d(sm + QO_KC + hb * KB_K, &tk, bar_in, 64 * hb, c0, unit);
-            tma_load_3d(sm + QO_V + (2 + hb) * TILE, &tv, bar_in, 64 * hb, c0, unit);
+            tma_load_3d(sm + QO_KC + hb * KB_K, &tk, bar_in, 64 * hb, c0, kvu);
+            tma_load_3d(sm + QO_V + (2 + hb) * TILE, &tv, bar_in, 64 * hb, c0, kvu);
             if (has_prev) {
-                tma_load_3d(sm + QO_KP + hb * TILE, &tk, bar_in, 64 * hb, c0 - C, unit);
-                tma_load_3d(sm + QO_V + hb * TILE, &tv, bar_in, 64 * hb, c0 - C, unit);
+                tma_load_3d(sm + QO_KP + hb * TILE, &tk, bar_in, 64 * hb, c0 - C, kvu);
+                tma_load_3d(sm + QO_V + hb * TILE, &tv, bar_in, 64 * hb, c0 - C, kvu);
             }
         }
         in_issued = 1;
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             float da = hs == 0 ? dot : 0.f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-            if (lane == 0) atomicAdd(a.dalpha, da);
+            if (lane == 0) atomicAdd(a.dalpha + (a.alpha_h ? h : 0), da);
             // dSC = P (alpha dP - D_t) over the band, dC = P_meta (0 - D_t)
             uint32_t r[4][16], rd[4][16], rm[16];
 #pragma unroll
@@ -785,9 +790,11 @@ struct KeyArgs {
     const __nv_bfloat16 *Sb;      // [units][nchunks][D][D]  state before chunk c
     const float *xq;              // [units][L][D]  q * dq_gate
     const float *lse2, *drow;     // [units][L]
-    __nv_bfloat16 *dk, *dv, *dg;  // [units][L][D]
+    __nv_bfloat16 *dk, *dv, *dg;  // [units][L][D]  (dk, dv per query head; summed over a group afterwards)
     float alpha;
     int L, w, nchunks;
+    const float *alpha_h;         // per-head anchor weights (null: alpha)
+    int H, group;                 // query heads per key/value head
 };
 
 // Shared memory of bwd_key_kernel.  Phase A (anchor products) uses the
@@ -838,7 +845,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int c0 = c * C, n = min(C, L - c0);
     const bool has_next = c + 1 < nch;
     const int nn = has_next ? min(C, L - c0 - C) : 0;  // rows of the next chunk
-    const float alpha = a.alpha;
+    const float alpha = head_alpha(a.alpha_h, a.alpha, unit % a.H);
+    const int kvu = kv_unit(unit, a.H, a.group);
 
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -858,8 +866,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(bar_in, (has_next ? 9 : 7) * 2 * TILE);
         for (int hb = 0; hb < 2; ++hb) {
             tma_load_3d(sm + KO_Q + hb * TILE, &tq, bar_in, 64 * hb, c0, unit);
-            tma_load_3d(sm + KO_K + hb * TILE, &tk, bar_in, 64 * hb, c0, unit);
-            tma_load_3d(sm + KO_V + hb * TILE, &tv, bar_in, 64 * hb, c0, unit);
+            tma_load_3d(sm + KO_K + hb * TILE, &tk, bar_in, 64 * hb, c0, kvu);
+            tma_load_3d(sm + KO_V + hb * TILE, &tv, bar_in, 64 * hb, c0, kvu);
             tma_load_3d(sm + KO_DY + hb * TILE, &tdy, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + KO_G + hb * TILE, &tg, bar_in, 64 * hb, c0, unit);
             if (has_next) {

@@ -54,6 +54,18 @@ __device__ __forceinline__ float warp_max(float x)
     return x;
 }
 
+// Grouped key/value heads: query head h of a batch row reads key/value head
+// h / group of that row (group = H / Hkv; 1 when every head has its own).
+__host__ __device__ __forceinline__ int kv_unit(int unit, int H, int group)
+{
+    return (unit / H) * (H / group) + (unit % H) / group;
+}
+// The anchor weight of head h: per head when alpha_h is given.
+__device__ __forceinline__ float head_alpha(const float *alpha_h, float alpha, int h)
+{
+    return alpha_h ? alpha_h[h] : alpha;
+}
+
 // Library-wide device error word.  A kernel that abandons a bounded wait,
 // or finds a state it cannot use, records a code here and skips the work;
 // the host reads and clears it (lizard_check_device_status).  The library is

@@ -35,6 +35,8 @@ struct DecodeArgs {
     const int64_t *pos;
     float alpha;
     int B, H, w, m;
+    const float *alpha_h;  // per-head anchor weights (null: alpha)
+    int group;             // query heads per key/value head (k, v are [B][H / group][D])
 };
 
 constexpr int DECODE_THREADS = 256;
@@ -161,10 +163,12 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
         dec_bulk_g2s(dsm + plan.ring_bytes, static_cast<const T *>(a.ring_v) + (size_t)u * w * D,
                      (uint32_t)plan.ring_bytes, bar);
         const void *src[4] = {a.q, a.k, a.v, a.g};
+        const size_t kvu = (size_t)kv_unit(u, H, a.group);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             dec_bulk_g2s(dsm + 2 * plan.ring_bytes + j * plan.tok_bytes,
-                         static_cast<const T *>(src[j]) + (size_t)u * D, (uint32_t)plan.tok_bytes, bar);
+                         static_cast<const T *>(src[j]) + (j == 1 || j == 2 ? kvu : (size_t)u) * D,
+                         (uint32_t)plan.tok_bytes, bar);
         if (plan.mu_copy)
             dec_bulk_g2s(dsm + 2 * plan.ring_bytes + 4 * plan.tok_bytes,
                          static_cast<const T *>(a.mu) + (size_t)(u % H) * m * D, plan.mu_copy, bar);
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
         Z = warp_sum(Z);
         if (lane == 0) {
             stat[0] = M;
-            stat[1] = a.alpha / Z;
+            stat[1] = head_alpha(a.alpha_h, a.alpha, u % H) / Z;
         }
     }
     __syncthreads();

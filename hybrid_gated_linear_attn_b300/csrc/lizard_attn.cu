@@ -151,16 +151,16 @@ static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
 
 static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
 {
-    const int units = pa.B * pa.H;
+    const int units = pa.B * pa.H, kv_units = pa.B * (pa.H / pa.group);
     CUtensorMap tq, tk, tv;
-    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
-        !make_token_map(&tv, pa.v, units, pa.L))
+    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
+        !make_token_map(&tv, pa.v, kv_units, pa.L))
         return LIZARD_ERR_CUDA;
     tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
-                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0};
+                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0, pa.alpha_h, pa.group};
     auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
                                                                           : tc::prefill_tc_kernel<2>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) != cudaSuccess)
@@ -216,9 +216,9 @@ static size_t segment_scratch_bytes(int units, int nseg, bool cont = false)
 // first segment reads.
 static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tg,
                                            float *scratch, int units, int L, int seg_chunks, int nseg,
-                                           const seg::ScanCont &sc, cudaStream_t s)
+                                           const seg::ScanCont &sc, int H, int group, cudaStream_t s)
 {
-    seg::SegArgs sa{scratch, scratch + (size_t)units * (nseg - 1) * ws::D * ws::D, L, seg_chunks, nseg};
+    seg::SegArgs sa{scratch, scratch + (size_t)units * (nseg - 1) * ws::D * ws::D, L, seg_chunks, nseg, H, group};
     if (cudaFuncSetAttribute(seg::segment_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)seg::SMEM_BYTES) != cudaSuccess)
         return LIZARD_ERR_CUDA;
@@ -243,9 +243,10 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
     const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
     nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
     if (nseg < 1) nseg = 1;
+    const int kv_units = pa.B * (pa.H / pa.group);
     CUtensorMap tq, tk, tv, tg;
-    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, units, pa.L) ||
-        !make_token_map(&tv, pa.v, units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
+    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
+        !make_token_map(&tv, pa.v, kv_units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
         return LIZARD_ERR_CUDA;
     float *seg_states = nullptr;
     bool owned = false;
@@ -278,14 +279,14 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
             seg0_state = copy;
             hist = hcopy;
         }
-        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, sc, s);
+        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, sc, pa.H, pa.group, s);
     }
     ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
                   static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
                   static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
                   nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg,
-                  pa.cont, seg0_state, hist};
+                  pa.cont, seg0_state, hist, pa.alpha_h, pa.group};
     if (rc == LIZARD_OK)
         rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units * nseg, s)
                        : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units * nseg, s);
@@ -318,6 +319,21 @@ static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
     return launch_status();
 }
 
+// Grouped key/value heads: sum the per-query-head dk, dv (ba.dk, ba.dv) of
+// each group into the key/value heads' outputs.
+template <typename T, int D>
+static lizard_status launch_gqa_reduce(const BackwardArgs &ba, void *dk_out, void *dv_out, cudaStream_t s)
+{
+    const long long LD = (long long)ba.L * D;
+    const long long n = (long long)ba.B * (ba.H / ba.group) * LD;
+    const int blocks = (int)(n / 256 + 1 < 148LL * 32 ? n / 256 + 1 : 148LL * 32);
+    gqa_reduce_kernel<T><<<blocks, 256, 0, s>>>(static_cast<const T *>(ba.dk), static_cast<T *>(dk_out), ba.B, ba.H,
+                                                 ba.group, LD);
+    gqa_reduce_kernel<T><<<blocks, 256, 0, s>>>(static_cast<const T *>(ba.dv), static_cast<T *>(dv_out), ba.B, ba.H,
+                                                 ba.group, LD);
+    return launch_status();
+}
+
 // Gradients: the two-sweep kernel over every unit, then the reduction of the
 // per-unit d mu and d alpha parts.  Scratch from the library's pool.
 template <typename T, int D>
@@ -327,17 +343,25 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
     const size_t xq_bytes = units * ba.L * D * sizeof(float);
     const size_t row_bytes = units * ba.L * sizeof(float);
     const size_t dmu_bytes = units * ba.m * D * sizeof(float);
-    const size_t bytes = xq_bytes + 2 * row_bytes + dmu_bytes + units * sizeof(float);
+    // grouped key/value heads: dk, dv per query head first, summed after
+    const size_t gqa_bytes = ba.group > 1 ? 2 * ((units * ba.L * D * sizeof(T) + 255) & ~(size_t)255) : 0;
+    const size_t bytes = gqa_bytes + xq_bytes + 2 * row_bytes + dmu_bytes + units * sizeof(float);
     uint8_t *scratch = nullptr;
     if (scratch_alloc(reinterpret_cast<void **>(&scratch), bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return LIZARD_ERR_CUDA;
     }
-    ba.xq = reinterpret_cast<float *>(scratch);
-    ba.lse = reinterpret_cast<float *>(scratch + xq_bytes);
-    ba.drow = reinterpret_cast<float *>(scratch + xq_bytes + row_bytes);
-    ba.dmu_part = reinterpret_cast<float *>(scratch + xq_bytes + 2 * row_bytes);
-    ba.dalpha_part = reinterpret_cast<float *>(scratch + xq_bytes + 2 * row_bytes + dmu_bytes);
+    void *dk_out = ba.dk, *dv_out = ba.dv;
+    if (gqa_bytes) {
+        ba.dk = scratch;
+        ba.dv = scratch + gqa_bytes / 2;
+    }
+    uint8_t *sc = scratch + gqa_bytes;
+    ba.xq = reinterpret_cast<float *>(sc);
+    ba.lse = reinterpret_cast<float *>(sc + xq_bytes);
+    ba.drow = reinterpret_cast<float *>(sc + xq_bytes + row_bytes);
+    ba.dmu_part = reinterpret_cast<float *>(sc + xq_bytes + 2 * row_bytes);
+    ba.dalpha_part = reinterpret_cast<float *>(sc + xq_bytes + 2 * row_bytes + dmu_bytes);
     lizard_status rc = LIZARD_OK;
     const size_t smem = backward_simt_smem_bytes<D>(ba.w, ba.m);
     auto kern = backward_simt_kernel<T, D>;
@@ -350,9 +374,10 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
     if (rc == LIZARD_OK) {
         const int mD = ba.m * D, n = ba.H * mD;
         backward_reduce_kernel<<<n > 0 ? (n + 255) / 256 : 1, 256, 0, s>>>(ba.dmu_part, ba.dalpha_part, ba.B, ba.H,
-                                                                           mD, dmu, dalpha);
+                                                                           mD, dmu, dalpha, ba.alpha_h != nullptr);
         rc = launch_status();
     }
+    if (rc == LIZARD_OK && gqa_bytes) rc = launch_gqa_reduce<T, D>(ba, dk_out, dv_out, s);
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -363,14 +388,23 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
 static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, float *dalpha, cudaStream_t s)
 {
     const int units = ba.B * ba.H, L = ba.L, nch = (L + bwdtc::C - 1) / bwdtc::C;
+    const int kv_units = ba.B * (ba.H / ba.group);
     const size_t D = bwdtc::D;
     const size_t st_bytes = (size_t)units * nch * D * D * sizeof(__nv_bfloat16);
     const size_t xq_bytes = (size_t)units * L * D * sizeof(float);
     const size_t row_bytes = ((size_t)units * L * sizeof(float) + 255) & ~(size_t)255;
+    // grouped key/value heads: dk, dv per query head first, summed after
+    const size_t gqa_bytes = ba.group > 1 ? 2 * (size_t)units * L * D * sizeof(__nv_bfloat16) : 0;
     uint8_t *scratch = nullptr;
-    if (scratch_alloc(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes, s) != cudaSuccess) {
+    if (scratch_alloc(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes + gqa_bytes, s) !=
+        cudaSuccess) {
         cudaGetLastError();
         return LIZARD_ERR_CUDA;
+    }
+    BackwardArgs bg = ba;
+    if (gqa_bytes) {
+        bg.dk = scratch + 2 * st_bytes + xq_bytes + 2 * row_bytes;
+        bg.dv = static_cast<uint8_t *>(bg.dk) + gqa_bytes / 2;
     }
     __nv_bfloat16 *Sb = reinterpret_cast<__nv_bfloat16 *>(scratch);
     __nv_bfloat16 *Ha = reinterpret_cast<__nv_bfloat16 *>(scratch + st_bytes);
@@ -379,16 +413,17 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     float *drow = reinterpret_cast<float *>(scratch + 2 * st_bytes + xq_bytes + row_bytes);
     lizard_status rc = LIZARD_OK;
     CUtensorMap tq, tk, tv, tg, tdy, tS, tH;
-    if (!make_token_map(&tq, ba.q, units, L) || !make_token_map(&tk, ba.k, units, L) ||
-        !make_token_map(&tv, ba.v, units, L) || !make_token_map(&tg, ba.g, units, L) ||
+    if (!make_token_map(&tq, ba.q, units, L) || !make_token_map(&tk, ba.k, kv_units, L) ||
+        !make_token_map(&tv, ba.v, kv_units, L) || !make_token_map(&tg, ba.g, units, L) ||
         !make_token_map(&tdy, ba.dy, units, L) || !make_token_map(&tS, Sb, units * nch, (int)D) ||
         !make_token_map(&tH, Ha, units * nch, (int)D))
         rc = LIZARD_ERR_CUDA;
-    if (rc == LIZARD_OK && cudaMemsetAsync(dalpha, 0, sizeof(float), s) != cudaSuccess) rc = LIZARD_ERR_CUDA;
+    if (rc == LIZARD_OK && cudaMemsetAsync(dalpha, 0, sizeof(float) * (ba.alpha_h ? ba.H : 1), s) != cudaSuccess)
+        rc = LIZARD_ERR_CUDA;
     if (rc == LIZARD_OK && dmu && cudaMemsetAsync(dmu, 0, sizeof(float) * ba.H * ba.m * D, s) != cudaSuccess)
         rc = LIZARD_ERR_CUDA;
     if (rc == LIZARD_OK) {
-        bwdtc::StatesArgs sa{Sb, Ha, static_cast<const __nv_bfloat16 *>(ba.g), L, nch};
+        bwdtc::StatesArgs sa{Sb, Ha, static_cast<const __nv_bfloat16 *>(ba.g), L, nch, ba.H, ba.group};
         if (cudaFuncSetAttribute(bwdtc::chunk_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::ST_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
@@ -400,7 +435,7 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     if (rc == LIZARD_OK) {
         bwdtc::QueryArgs qa{static_cast<const __nv_bfloat16 *>(ba.mu), static_cast<const __nv_bfloat16 *>(ba.k),
                             static_cast<__nv_bfloat16 *>(ba.dq), xq, lse2, drow, dmu, dalpha, ba.alpha, ba.H, L,
-                            ba.w, ba.m, nch};
+                            ba.w, ba.m, nch, ba.alpha_h, ba.group};
         if (cudaFuncSetAttribute(bwdtc::bwd_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::QO_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
@@ -410,8 +445,8 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
         }
     }
     if (rc == LIZARD_OK) {
-        bwdtc::KeyArgs ka{Sb, xq, lse2, drow, static_cast<__nv_bfloat16 *>(ba.dk), static_cast<__nv_bfloat16 *>(ba.dv),
-                          static_cast<__nv_bfloat16 *>(ba.dg), ba.alpha, L, ba.w, nch};
+        bwdtc::KeyArgs ka{Sb, xq, lse2, drow, static_cast<__nv_bfloat16 *>(bg.dk), static_cast<__nv_bfloat16 *>(bg.dv),
+                          static_cast<__nv_bfloat16 *>(ba.dg), ba.alpha, L, ba.w, nch, ba.alpha_h, ba.H, ba.group};
         if (cudaFuncSetAttribute(bwdtc::bwd_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::KO_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
@@ -420,6 +455,7 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
             rc = launch_status();
         }
     }
+    if (rc == LIZARD_OK && gqa_bytes) rc = launch_gqa_reduce<__nv_bfloat16, 128>(bg, ba.dk, ba.dv, s);
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -498,12 +534,38 @@ lizard_status lizard_state_init(const lizard_state *st, lizard_stream_t stream)
     return launch_status();
 }
 
+// A variant's key/value grouping and per-head weights, validated.
+static lizard_status variant_of(const lizard_variant *var, int H, int *group, const float **alpha_h)
+{
+    *group = 1;
+    *alpha_h = nullptr;
+    if (!var) return LIZARD_OK;
+    const int Hkv = var->Hkv == 0 ? H : var->Hkv;
+    if (Hkv < 1 || Hkv > H || H % Hkv != 0) return LIZARD_ERR_INVALID_ARG;
+    if (var->alpha_h && (reinterpret_cast<uintptr_t>(var->alpha_h) & 3u)) return LIZARD_ERR_INVALID_ARG;
+    *group = H / Hkv;
+    *alpha_h = var->alpha_h;
+    return LIZARD_OK;
+}
+
 lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
                                   float alpha, int B, int H, int L, int dk, int dv, int w, int m,
                                   lizard_dtype dtype, void *y, const lizard_state *st, lizard_stream_t stream)
 {
+    return lizard_attn_prefill_v(q, k, v, g, meta_k, alpha, B, H, L, dk, dv, w, m, dtype, y, st, nullptr, stream);
+}
+
+lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
+                                    float alpha, int B, int H, int L, int dk, int dv, int w, int m,
+                                    lizard_dtype dtype, void *y, const lizard_state *st, const lizard_variant *var,
+                                    lizard_stream_t stream)
+{
     if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
     if (B < 0 || H < 1 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0) return LIZARD_ERR_INVALID_ARG;
+    int group = 1;
+    const float *alpha_h = nullptr;
+    lizard_status vrc = variant_of(var, H, &group, &alpha_h);
+    if (vrc != LIZARD_OK) return vrc;
     // An empty prompt (L == 0) has no token tensors to point at.
     if (L > 0 && (!q || !k || !v || !g || !y)) return LIZARD_ERR_INVALID_ARG;
     if (m > 0 && !meta_k) return LIZARD_ERR_INVALID_ARG;
@@ -523,7 +585,7 @@ lizard_status lizard_attn_prefill(const void *q, const void *k, const void *v, c
     if (L == 0) return st ? lizard_state_init(st, stream) : LIZARD_OK;  // the empty prompt leaves the empty state
     PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m,
                    st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
-                   st ? st->pos : nullptr};
+                   st ? st->pos : nullptr, 0, nullptr, alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == LIZARD_BF16)
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
@@ -559,7 +621,7 @@ lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const vo
     if (rc != LIZARD_OK) return rc;
     PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m,
                    st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
-                   st ? st->pos : nullptr};
+                   st ? st->pos : nullptr, 0, nullptr, nullptr, 1};
     // Segment states beyond LIZARD_NOALLOC_SCRATCH_BYTES: LIZARD_ERR_UNSUPPORTED, nothing launched.
     return launch_prefill_ws(pa, (cudaStream_t)stream, scratch, LIZARD_NOALLOC_SCRATCH_BYTES);
 }
@@ -568,7 +630,18 @@ lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const v
                                           const void *meta_k, float alpha, int L, int m, void *y,
                                           const lizard_state *st, lizard_stream_t stream)
 {
+    return lizard_attn_prefill_continue_v(q, k, v, g, meta_k, alpha, L, m, y, st, nullptr, stream);
+}
+
+lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const void *v, const void *g,
+                                            const void *meta_k, float alpha, int L, int m, void *y,
+                                            const lizard_state *st, const lizard_variant *var, lizard_stream_t stream)
+{
     lizard_status rc = check_state(st);
+    if (rc != LIZARD_OK) return rc;
+    int group = 1;
+    const float *alpha_h = nullptr;
+    rc = variant_of(var, st->H, &group, &alpha_h);
     if (rc != LIZARD_OK) return rc;
     if (L < 0 || m < 0) return LIZARD_ERR_INVALID_ARG;
     if (L > 0 && (!q || !k || !v || !g || !y)) return LIZARD_ERR_INVALID_ARG;
@@ -583,7 +656,8 @@ lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const v
     // (H x segments of at most the SM count must stay below 2^23).
     if (H > 16384) return LIZARD_ERR_UNSUPPORTED;
     if (B == 0 || L == 0) return LIZARD_OK;  // no new token: the state stays as it is
-    PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m, st->S, st->ring_k, st->ring_v, st->pos, 1, st->S};
+    PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m, st->S, st->ring_k, st->ring_v, st->pos, 1, st->S,
+                   alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
@@ -596,8 +670,21 @@ lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, 
                                    const void *dy, void *dq, void *dk_out, void *dv_out, void *dg, float *dmeta_k,
                                    float *dalpha, lizard_stream_t stream)
 {
+    return lizard_attn_backward_v(q, k, v, g, meta_k, alpha, B, H, L, dk, dv, w, m, dtype, dy, dq, dk_out, dv_out, dg,
+                                  dmeta_k, dalpha, nullptr, stream);
+}
+
+lizard_status lizard_attn_backward_v(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
+                                     float alpha, int B, int H, int L, int dk, int dv, int w, int m, lizard_dtype dtype,
+                                     const void *dy, void *dq, void *dk_out, void *dv_out, void *dg, float *dmeta_k,
+                                     float *dalpha, const lizard_variant *var, lizard_stream_t stream)
+{
     if (!dtype_ok(dtype)) return LIZARD_ERR_INVALID_ARG;
     if (B < 0 || H < 1 || L < 0 || dk < 1 || dv < 1 || w < 1 || m < 0) return LIZARD_ERR_INVALID_ARG;
+    int group = 1;
+    const float *alpha_h = nullptr;
+    lizard_status vrc = variant_of(var, H, &group, &alpha_h);
+    if (vrc != LIZARD_OK) return vrc;
     if (L > 0 && B > 0 && (!q || !k || !v || !g || !dy || !dq || !dk_out || !dv_out || !dg))
         return LIZARD_ERR_INVALID_ARG;
     if (m > 0 && (!meta_k || !dmeta_k)) return LIZARD_ERR_INVALID_ARG;
@@ -610,12 +697,12 @@ lizard_status lizard_attn_backward(const void *q, const void *k, const void *v, 
     if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     if (B == 0 || L == 0) {  // no token: the parameter gradients are zero
-        if (cudaMemsetAsync(dalpha, 0, sizeof(float), s) != cudaSuccess) return LIZARD_ERR_CUDA;
+        if (cudaMemsetAsync(dalpha, 0, sizeof(float) * (alpha_h ? H : 1), s) != cudaSuccess) return LIZARD_ERR_CUDA;
         if (m > 0 && cudaMemsetAsync(dmeta_k, 0, sizeof(float) * H * m * dk, s) != cudaSuccess) return LIZARD_ERR_CUDA;
         return LIZARD_OK;
     }
     BackwardArgs ba{q, k, v, g, meta_k, dy, dq, dk_out, dv_out, dg, alpha, B, H, L, w, m,
-                    nullptr, nullptr, nullptr, nullptr, nullptr};
+                    nullptr, nullptr, nullptr, nullptr, nullptr, alpha_h, group};
     float *dmu = m > 0 ? dmeta_k : nullptr;
     if (dtype == LIZARD_BF16 && dk == 128 && w <= 65) return launch_backward_tc(ba, dmu, dalpha, s);
     if (dtype == LIZARD_BF16)
@@ -655,7 +742,18 @@ lizard_status lizard_gate_projection(const void *x, const void *w_gamma, int B, 
 lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g, const void *meta_k,
                                       float alpha, int m, void *y, const lizard_state *st, lizard_stream_t stream)
 {
+    return lizard_attn_decode_step_v(q, k, v, g, meta_k, alpha, m, y, st, nullptr, stream);
+}
+
+lizard_status lizard_attn_decode_step_v(const void *q, const void *k, const void *v, const void *g,
+                                        const void *meta_k, float alpha, int m, void *y, const lizard_state *st,
+                                        const lizard_variant *var, lizard_stream_t stream)
+{
     lizard_status rc = check_state(st);
+    if (rc != LIZARD_OK) return rc;
+    int group = 1;
+    const float *alpha_h = nullptr;
+    rc = variant_of(var, st->H, &group, &alpha_h);
     if (rc != LIZARD_OK) return rc;
     if (m < 0) return LIZARD_ERR_INVALID_ARG;
     if (!q || !k || !v || !g || !y || (m > 0 && !meta_k)) return LIZARD_ERR_INVALID_ARG;
@@ -664,7 +762,8 @@ lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *
         return LIZARD_ERR_INVALID_ARG;
     if (m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
     if (st->B == 0) return LIZARD_OK;
-    DecodeArgs da{q, k, v, g, meta_k, y, st->S, st->ring_k, st->ring_v, st->pos, alpha, st->B, st->H, st->w, m};
+    DecodeArgs da{q, k, v, g, meta_k, y, st->S, st->ring_k, st->ring_v, st->pos, alpha, st->B, st->H, st->w, m,
+                  alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
         return st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s) : launch_decode<__nv_bfloat16, 64>(da, s);

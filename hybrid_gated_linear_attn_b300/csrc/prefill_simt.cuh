@@ -38,6 +38,10 @@ struct PrefillArgs {
     // unit's S0 before it writes S_out).
     int cont;
     const float *S0;
+    // Variants: per-head anchor weights alpha_h[H] (null: alpha for every
+    // head) and grouped key/value heads (k, v hold B x H / group heads).
+    const float *alpha_h;
+    int group;
 };
 
 constexpr int SIMT_C = 64;        // chunk length
@@ -74,8 +78,9 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
 
     const size_t base = (size_t)unit * L * D;
     const T *q = static_cast<const T *>(a.q) + base;
-    const T *k = static_cast<const T *>(a.k) + base;
-    const T *v = static_cast<const T *>(a.v) + base;
+    const size_t kvbase = (size_t)kv_unit(unit, a.H, a.group) * L * D;
+    const T *k = static_cast<const T *>(a.k) + kvbase;
+    const T *v = static_cast<const T *>(a.v) + kvbase;
     const T *g = static_cast<const T *>(a.g) + base;
     const T *mu = static_cast<const T *>(a.mu) + (size_t)h * m * D;
     T *y = static_cast<T *>(a.y) + base;
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(SIMT_THREADS, 1) prefill_simt_kernel(PrefillAr
             float Z = 0.f;
             for (int c = lane; c < nk + m; c += 32) Z += expf(sc[c] - M);
             Z = warp_sum(Z);
-            const float scale = a.alpha / Z;
+            const float scale = head_alpha(a.alpha_h, a.alpha, h) / Z;
             for (int c = 0; c < nk; ++c) {
                 const int tau = first + c;
                 const float pc = expf(sc[c] - M) * scale;

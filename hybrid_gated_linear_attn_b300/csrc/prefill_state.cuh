@@ -54,6 +54,7 @@ struct SegArgs {
     float *dS;      // [units][nseg-1][D][D] fp32, row = key dim
     float *lam;     // [units][nseg-1][D] fp32 (base-2 log of the segment's decay)
     int L, seg_chunks, nseg;
+    int H, group;   // query heads per key/value head (tk, tv map B x H / group heads)
 };
 
 // grid = units * (nseg - 1): CTA (unit, p) covers chunks [p * seg_chunks, (p+1) * seg_chunks).
@@ -119,10 +120,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_expect_tx(&full[s], 3 * 2 * KB_T);
                 tma_load_3d(base, &tg, &full[s], 0, c * C, unit);
                 tma_load_3d(base + KB_T, &tg, &full[s], 64, c * C, unit);
-                tma_load_3d(base + 2 * KB_T, &tk, &full[s], 0, c * C, unit);
-                tma_load_3d(base + 3 * KB_T, &tk, &full[s], 64, c * C, unit);
-                tma_load_3d(base + 4 * KB_T, &tv, &full[s], 0, c * C, unit);
-                tma_load_3d(base + 5 * KB_T, &tv, &full[s], 64, c * C, unit);
+                tma_load_3d(base + 2 * KB_T, &tk, &full[s], 0, c * C, kv_unit(unit, a.H, a.group));
+                tma_load_3d(base + 3 * KB_T, &tk, &full[s], 64, c * C, kv_unit(unit, a.H, a.group));
+                tma_load_3d(base + 4 * KB_T, &tv, &full[s], 0, c * C, kv_unit(unit, a.H, a.group));
+                tma_load_3d(base + 5 * KB_T, &tv, &full[s], 64, c * C, kv_unit(unit, a.H, a.group));
                 ++issued[s];
             }
             for (int s = 0; s < ST; ++s)

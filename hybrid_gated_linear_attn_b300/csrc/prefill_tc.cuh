@@ -95,6 +95,8 @@ struct TcArgs {
     // the CTA reads it before it writes S_out).
     int cont;
     const float *S0;
+    const float *alpha_h;  // per-head anchor weights (null: alpha)
+    int group;             // query heads per key/value head (maps tk, tv over B x H / group heads)
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // (chunks -NH .. -1), of which tokens -nvalid .. -1 are keys.  Chunk c
     // lives in k/v slot (c + NH) % NR.
     const int NH = a.cont ? NP : 0;
+    const int kvu = kv_unit(unit, a.H, a.group);  // this head's key/value head
     // Prep mapping: key dims 2ip and 2ip+1, tokens 16*tqr .. 16*tqr+15.
     const int ip = tid & 63, tqr = tid >> 6;
     // Softmax mapping (M = 64 accumulator layout): row srow, column part 2*half + ssub.
@@ -243,10 +246,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = (c + NH) % NR;
         uint8_t *base = sm + OFF_KV + s * KV_SLOT;
         mbar_arrive_expect_tx(&bar_kv[s], 4 * TILE);
-        tma_load_3d(base, &tk, &bar_kv[s], 0, c * C, unit);
-        tma_load_3d(base + TILE, &tk, &bar_kv[s], 64, c * C, unit);
-        tma_load_3d(base + V_OFF, &tv, &bar_kv[s], 0, c * C, unit);
-        tma_load_3d(base + V_OFF + TILE, &tv, &bar_kv[s], 64, c * C, unit);
+        tma_load_3d(base, &tk, &bar_kv[s], 0, c * C, kvu);
+        tma_load_3d(base + TILE, &tk, &bar_kv[s], 64, c * C, kvu);
+        tma_load_3d(base + V_OFF, &tv, &bar_kv[s], 0, c * C, kvu);
+        tma_load_3d(base + V_OFF + TILE, &tv, &bar_kv[s], 64, c * C, kvu);
         ++issued[B_KV + s];
     };
     if (tid == 0 && nchunks > 0) {
@@ -502,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
             if (ssub == 0) red[128 + half * 64 + t] = sum;
             __syncthreads();
-            const float inv = a.alpha / (red[128 + t] + red[192 + t]);
+            const float inv = head_alpha(a.alpha_h, a.alpha, h) / (red[128 + t] + red[192 + t]);
 #pragma unroll
             for (int gq = 0; gq < NB; ++gq) {
                 const int colw = 2 * PART * half + 16 * gq;  // band column of lanes 0..15 (lanes 16..31: + PART)
@@ -642,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         const int first = max(0, L - w);
-        const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
+        const __nv_bfloat16 *kp = a.k + (size_t)kvu * L * D, *vp = a.v + (size_t)kvu * L * D;
         __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
         for (int e = tid; e < (L - first) * D; e += THREADS) {
             const int tau = first + e / D, i = e % D;

@@ -122,6 +122,8 @@ struct WsArgs {
     int cont;
     const float *S0;
     const __nv_bfloat16 *hist;
+    const float *alpha_h;  // per-head anchor weights (null: alpha)
+    int group;             // query heads per key/value head (tk, tv map B x H / group heads)
 };
 
 // ---------------------------------------------------------------- helpers
@@ -336,6 +338,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // memory only after the barrier above), and the history tokens
     // -nvalid .. -1 in the window.
     const int64_t p0 = a.cont ? *p0_slot : 0;
+    const int kvu = kv_unit(unit, a.H, a.group);  // this head's key/value head
     const int nvalid = a.cont ? (int)min(p0, (int64_t)(w - 1)) : 0;
     if (c_lo < 0) {
         // Window history (chunk -1) into k/v slot 0, zero rows where no key,
@@ -391,11 +394,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive(&v_full[s]);
                 } else {
                     mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                    tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
-                    tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                    tma_load_3d(base, &tk, &k_full[s], 0, c * C, kvu);
+                    tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, kvu);
                     mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                    tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
-                    tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                    tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, kvu);
+                    tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, kvu);
                 }
                 ++k_issued[s];
                 ++v_issued[s];
@@ -411,8 +414,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t *base = sm + SM::KV + s * SLOT;
                 if (r >= NR && !bwait(&k_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                tma_load_3d(base, &tk, &k_full[s], 0, c * C, unit);
-                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, unit);
+                tma_load_3d(base, &tk, &k_full[s], 0, c * C, kvu);
+                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, kvu);
                 ++k_issued[s];
                 const int qs = pc % QS;
                 if (pc >= QS && !bwait(&q_empty[qs], pc / QS - 1, abort_f)) { give_up(); break; }
@@ -422,8 +425,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ++q_issued[qs];
                 if (r >= NR && !bwait(&v_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, unit);
-                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, unit);
+                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, kvu);
+                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, kvu);
                 ++v_issued[s];
             }
             // Drain: every copy issued has landed before shared memory is released.
@@ -792,7 +795,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // prompt advanced pos at its start).
         if (!failed && a.S_out && last_seg) {
             const int first = max(0, L - w);
-            const __nv_bfloat16 *kp = a.k + (size_t)unit * L * D, *vp = a.v + (size_t)unit * L * D;
+            const __nv_bfloat16 *kp = a.k + (size_t)kvu * L * D, *vp = a.v + (size_t)kvu * L * D;
             __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
             for (int e = tp; e < (L - first) * (D / 8); e += PREP_N) {
                 const int tau = first + e / (D / 8), i8 = (e % (D / 8)) * 8;
@@ -865,7 +868,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int e = 0; e < META_ROWS; ++e)
                 if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            const float inv = a.alpha / sum;
+            const float inv = head_alpha(a.alpha_h, a.alpha, h) / sum;
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
                            [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
                 give_up();

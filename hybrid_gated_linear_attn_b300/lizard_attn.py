@@ -23,15 +23,27 @@ LIZARD_F32, LIZARD_BF16 = 0, 1
 LIZARD_MAX_WINDOW = 128
 LIZARD_MAX_META = 16
 
-EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
-           "lizard_attn_backward", "lizard_gate_projection", "lizard_attn_decode_step", "lizard_check_device_status",
-           "lizard_status_string")
+EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_v", "lizard_attn_prefill_continue",
+           "lizard_attn_prefill_continue_v", "lizard_attn_prefill_noalloc", "lizard_attn_backward",
+           "lizard_attn_backward_v", "lizard_gate_projection", "lizard_attn_decode_step", "lizard_attn_decode_step_v",
+           "lizard_check_device_status", "lizard_status_string")
 
 
 class LizardError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {status_name(status)}")
+
+
+class lizard_variant(ctypes.Structure):
+    _fields_ = [("alpha_h", ctypes.c_void_p), ("Hkv", ctypes.c_int)]
+
+
+def _variant(alpha_h=None, Hkv=0):
+    """A lizard_variant by reference, or None for the plain operator."""
+    if alpha_h is None and not Hkv:
+        return None
+    return ctypes.byref(lizard_variant(alpha_h.data_ptr() if alpha_h is not None else None, int(Hkv)))
 
 
 class lizard_state(ctypes.Structure):
@@ -58,8 +70,17 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         SP = ctypes.POINTER(lizard_state)
         lib.lizard_state_init.argtypes = [SP, P]
         lib.lizard_state_init.restype = I
+        VP = ctypes.POINTER(lizard_variant)
         lib.lizard_attn_prefill.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
         lib.lizard_attn_prefill.restype = I
+        lib.lizard_attn_prefill_v.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, VP, P]
+        lib.lizard_attn_prefill_v.restype = I
+        lib.lizard_attn_prefill_continue_v.argtypes = [P, P, P, P, P, F, I, I, P, SP, VP, P]
+        lib.lizard_attn_prefill_continue_v.restype = I
+        lib.lizard_attn_backward_v.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, VP, P]
+        lib.lizard_attn_backward_v.restype = I
+        lib.lizard_attn_decode_step_v.argtypes = [P, P, P, P, P, F, I, P, SP, VP, P]
+        lib.lizard_attn_decode_step_v.restype = I
         lib.lizard_attn_prefill_continue.argtypes = [P, P, P, P, P, F, I, I, P, SP, P]
         lib.lizard_attn_prefill_continue.restype = I
         lib.lizard_attn_prefill_noalloc.argtypes = [P, P, P, P, P, F, I, I, I, I, I, I, I, I, P, SP, P]
@@ -132,10 +153,12 @@ def lizard_state_init(state: LizardState, stream=None) -> LizardState:
 
 
 def lizard_attn_prefill(q, k, v, g, meta_k, alpha, w, y=None, state: LizardState | None = None,
-                        stream=None) -> torch.Tensor:
+                        stream=None, alpha_h=None, Hkv=0) -> torch.Tensor:
     """y = Lizard(q, k, v, g; meta_k, alpha, w) over [B,H,L,d] tensors.
 
-    ``state``, when given, receives the state after the prompt.
+    ``state``, when given, receives the state after the prompt.  ``alpha_h``
+    (a [H] fp32 device tensor) and ``Hkv`` select the variants of
+    ``lizard_variant`` (k, v then [B,Hkv,L,d]).
     """
     B, H, L, dk = q.shape
     dv = v.shape[-1]
@@ -143,16 +166,16 @@ def lizard_attn_prefill(q, k, v, g, meta_k, alpha, w, y=None, state: LizardState
     if y is None:
         y = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
     st = state.c_struct() if state is not None else None
-    rc = library().lizard_attn_prefill(
+    rc = library().lizard_attn_prefill_v(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha),
         B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(y),
-        ctypes.byref(st) if st is not None else None, _stream(stream))
+        ctypes.byref(st) if st is not None else None, _variant(alpha_h, Hkv), _stream(stream))
     _check(rc, "lizard_attn_prefill")
     return y
 
 
 def lizard_attn_prefill_continue(q, k, v, g, meta_k, alpha, state: LizardState, y=None,
-                                 stream=None) -> torch.Tensor:
+                                 stream=None, alpha_h=None, Hkv=0) -> torch.Tensor:
     """L more tokens per sequence ([B,H,L,d] tensors), continuing from
     ``state`` (updated in place): the window and the gate state carry on
     from the tokens the state has already consumed."""
@@ -161,9 +184,9 @@ def lizard_attn_prefill_continue(q, k, v, g, meta_k, alpha, state: LizardState, 
     if y is None:
         y = torch.empty(state.B, state.H, L, state.dv, dtype=q.dtype, device=q.device)
     st = state.c_struct()
-    rc = library().lizard_attn_prefill_continue(
+    rc = library().lizard_attn_prefill_continue_v(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha), L, m,
-        _ptr(y), ctypes.byref(st), _stream(stream))
+        _ptr(y), ctypes.byref(st), _variant(alpha_h, Hkv), _stream(stream))
     _check(rc, "lizard_attn_prefill_continue")
     return y
 
@@ -187,7 +210,7 @@ def lizard_attn_prefill_noalloc(q, k, v, g, meta_k, alpha, w, y=None, state: Liz
     return y
 
 
-def lizard_attn_backward(q, k, v, g, meta_k, alpha, w, dy, stream=None):
+def lizard_attn_backward(q, k, v, g, meta_k, alpha, w, dy, stream=None, alpha_h=None, Hkv=0):
     """Gradients of sum(dy * y) through the operator over [B,H,L,d] tensors
     that start from the empty state.  Returns (dq, dk, dv, dg, dmeta_k,
     dalpha): the first four in the input dtype, dmeta_k [H,m,dk] fp32 (None
@@ -195,14 +218,14 @@ def lizard_attn_backward(q, k, v, g, meta_k, alpha, w, dy, stream=None):
     B, H, L, dk = q.shape
     dv = v.shape[-1]
     m = meta_k.shape[1] if meta_k is not None else 0
-    dq, dk_, dg = (torch.empty_like(q) for _ in range(3))
-    dv_ = torch.empty_like(v)
+    dq, dg = torch.empty_like(q), torch.empty_like(g)
+    dk_, dv_ = torch.empty_like(k), torch.empty_like(v)
     dmeta = torch.empty(H, m, dk, dtype=torch.float32, device=q.device) if m > 0 else None
-    dalpha = torch.empty((), dtype=torch.float32, device=q.device)
-    rc = library().lizard_attn_backward(
+    dalpha = torch.empty((H,) if alpha_h is not None else (), dtype=torch.float32, device=q.device)
+    rc = library().lizard_attn_backward_v(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha),
         B, H, L, dk, dv, int(w), m, _dtype_code(q), _ptr(dy), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg),
-        _ptr(dmeta) if m > 0 else None, _ptr(dalpha), _stream(stream))
+        _ptr(dmeta) if m > 0 else None, _ptr(dalpha), _variant(alpha_h, Hkv), _stream(stream))
     _check(rc, "lizard_attn_backward")
     return dq, dk_, dv_, dg, dmeta, dalpha
 
@@ -220,15 +243,16 @@ def lizard_gate_projection(x, w_gamma, H, g=None, stream=None) -> torch.Tensor:
     return g
 
 
-def lizard_attn_decode_step(q, k, v, g, meta_k, alpha, state: LizardState, y=None, stream=None) -> torch.Tensor:
+def lizard_attn_decode_step(q, k, v, g, meta_k, alpha, state: LizardState, y=None, stream=None,
+                            alpha_h=None, Hkv=0) -> torch.Tensor:
     """One token per sequence: q,k,g [B,H,dk], v [B,H,dv] -> y [B,H,dv]."""
     m = meta_k.shape[1] if meta_k is not None else 0
     if y is None:
         y = torch.empty(state.B, state.H, state.dv, dtype=q.dtype, device=q.device)
     st = state.c_struct()
-    rc = library().lizard_attn_decode_step(
+    rc = library().lizard_attn_decode_step_v(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(meta_k) if m > 0 else None, float(alpha), m,
-        _ptr(y), ctypes.byref(st), _stream(stream))
+        _ptr(y), ctypes.byref(st), _variant(alpha_h, Hkv), _stream(stream))
     _check(rc, "lizard_attn_decode_step")
     return y
 

@@ -94,6 +94,27 @@ typedef struct {
 } lizard_state;
 
 /*
+ * Variants of the operator (the teachers' model shapes; the pages print
+ * neither, so both are design variants).  Passed to the *_v entry points;
+ * NULL there, or the plain entry points, mean neither.
+ *   alpha_h  [H] fp32 device array: the anchor weight of each head (the
+ *            combine y = yg + alpha_h[h] ya of gist.science/de section 2
+ *            item 3, per head); NULL: the call's alpha for every head.
+ *            4-byte aligned.
+ *   Hkv      key/value heads, 0 meaning H.  H % Hkv == 0: query head h
+ *            reads key/value head h / (H / Hkv) of its batch row, so k and
+ *            v (and, in the backward, dk and dv) are [B][Hkv][L][d] (decode:
+ *            [B][Hkv][d]).  The gate logits, the meta keys and the state
+ *            stay per query head (the state's ring keeps each query head's
+ *            window keys and values).
+ * An invalid variant (Hkv not dividing H, negative) is LIZARD_ERR_INVALID_ARG.
+ */
+typedef struct {
+    const float *alpha_h;
+    int Hkv;
+} lizard_variant;
+
+/*
  * lizard_state_init: the empty state -- S = 0, ring = 0, pos = 0 -- for all
  * B x H units.  Enqueued on `stream`.  Errors: INVALID_ARG for a null state
  * or buffer, bad sizes or misaligned buffers; CUDA if the launch fails.
@@ -120,6 +141,12 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
                                   int B, int H, int L, int dk, int dv, int w, int m,
                                   lizard_dtype dtype, void *y, const lizard_state *st,
                                   lizard_stream_t stream);
+
+/* lizard_attn_prefill with a variant (see lizard_variant). */
+LIZARD_API lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v, const void *g,
+                                    const void *meta_k, float alpha, int B, int H, int L, int dk, int dv,
+                                    int w, int m, lizard_dtype dtype, void *y, const lizard_state *st,
+                                    const lizard_variant *var, lizard_stream_t stream);
 
 /*
  * lizard_attn_prefill_continue: L more tokens of each of st->B sequences
@@ -155,6 +182,12 @@ LIZARD_API lizard_status lizard_attn_prefill(const void *q, const void *k, const
 LIZARD_API lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const void *v, const void *g,
                                            const void *meta_k, float alpha, int L, int m, void *y,
                                            const lizard_state *st, lizard_stream_t stream);
+
+/* lizard_attn_prefill_continue with a variant (see lizard_variant). */
+LIZARD_API lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const void *v, const void *g,
+                                             const void *meta_k, float alpha, int L, int m, void *y,
+                                             const lizard_state *st, const lizard_variant *var,
+                                             lizard_stream_t stream);
 
 /*
  * lizard_attn_prefill_noalloc: lizard_attn_prefill for callers that must not
@@ -216,6 +249,18 @@ LIZARD_API lizard_status lizard_attn_backward(const void *q, const void *k, cons
                                    lizard_stream_t stream);
 
 /*
+ * lizard_attn_backward with a variant (see lizard_variant).  With alpha_h,
+ * dalpha has H entries, d alpha_h[h] (each summed over the batch); with
+ * grouped key/value heads, dk and dv are [B][Hkv][L][d], each the sum over
+ * its group's query heads (fp32 sum of the heads' values, rounded once).
+ */
+LIZARD_API lizard_status lizard_attn_backward_v(const void *q, const void *k, const void *v, const void *g,
+                                     const void *meta_k, float alpha, int B, int H, int L, int dk, int dv,
+                                     int w, int m, lizard_dtype dtype, const void *dy, void *dq, void *dk_out,
+                                     void *dv_out, void *dg, float *dmeta_k, float *dalpha,
+                                     const lizard_variant *var, lizard_stream_t stream);
+
+/*
  * lizard_gate_projection: the gate logits the operator takes, from the layer
  * input -- the gate module Gamma = sigmoid(W_gamma x) of gist.science/de
  * section 2 item 1 sits directly ahead of the operator; this computes its
@@ -250,6 +295,12 @@ LIZARD_API lizard_status lizard_gate_projection(const void *x, const void *w_gam
 LIZARD_API lizard_status lizard_attn_decode_step(const void *q, const void *k, const void *v, const void *g,
                                       const void *meta_k, float alpha, int m, void *y,
                                       const lizard_state *st, lizard_stream_t stream);
+
+/* lizard_attn_decode_step with a variant (see lizard_variant). */
+LIZARD_API lizard_status lizard_attn_decode_step_v(const void *q, const void *k, const void *v, const void *g,
+                                        const void *meta_k, float alpha, int m, void *y,
+                                        const lizard_state *st, const lizard_variant *var,
+                                        lizard_stream_t stream);
 
 /*
  * lizard_check_device_status: synchronises `stream`, then reads and clears
