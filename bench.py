@@ -465,6 +465,13 @@ def run_profile_case(args):
         y = torch.empty_like(v)
         st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
         fn = lambda: lizard_attn_prefill(q, k, v, g, mu, wl.alpha, wl.w, y=y, state=st)  # noqa: E731
+    elif args.profile_case == "gate_projection":
+        from hybrid_gated_linear_attn_b300 import lizard_gate_projection
+        from hybrid_gated_linear_attn_b300.inputs import gate_projection_inputs
+        proj = gate_projection_inputs(wl.B, wl.L, 4096, wl.H, wl.dk)
+        px, pw = proj["x"].cuda(), proj["W"].cuda()
+        pg = torch.empty(wl.B, wl.H, wl.L, wl.dk, dtype=torch.bfloat16, device="cuda")
+        fn = lambda: lizard_gate_projection(px, pw, wl.H, g=pg)  # noqa: E731
     elif args.profile_case == "backward":
         inp = prefill_inputs(wl)
         q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
@@ -494,7 +501,7 @@ def main(argv=None):
     ap.add_argument("--sample-heads", type=int, default=None,
                     help="(batch, head) units in the oracle's timed sample (default: the whole workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "backward"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "backward", "gate_projection"], default=None,
                     help="only launch this operator W + K times (a small program for ncu); no JSON line")
     ap.add_argument("--workload", default=None, help="workload of --profile-case (default: the bench's)")
     ap.add_argument("--batch", type=int, default=0, help="batch override for --profile-case")

@@ -813,6 +813,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int t = 16 * quarter + (lane & 15);
         const uint32_t tl = tmem + tlane(quarter);
         const int st_ = tid - W_SOFT * 32;
+        const float alpha = head_alpha(a.alpha_h, a.alpha, h);  // this head's anchor weight
         for (int c = c_begin; c < c_end; ++c) {
             const int pc = c - c_begin;
             const int c0 = c * C, n = min(C, L - c0);
@@ -868,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int e = 0; e < META_ROWS; ++e)
                 if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            const float inv = head_alpha(a.alpha_h, a.alpha, h) / sum;
+            const float inv = alpha / sum;
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
                            [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
                 give_up();
