@@ -195,3 +195,32 @@ def test_gate_projection_rejects(lib, kw, code):
 
 def test_gate_projection_empty_is_ok(lib):
     assert gproj(lib, x=None, w=None, g=None, L=0) == OK
+
+
+def variant(alpha_h=None, Hkv=0):
+    return ctypes.byref(LA.lizard_variant(alpha_h, Hkv))
+
+
+@pytest.mark.parametrize("var,code", [
+    (dict(Hkv=3), INVALID),          # does not divide H = 4
+    (dict(Hkv=-1), INVALID),
+    (dict(Hkv=5), INVALID),          # more key/value heads than query heads
+    (dict(alpha_h=A + 2), INVALID),  # misaligned per-head weights
+])
+def test_variant_rejected_by_every_entry_point(lib, var, code):
+    v = variant(**var)
+    assert lib.lizard_attn_prefill_v(A, A, A, A, A, 1.0, 2, 4, 128, 128, 128, 64, 4, LA.LIZARD_BF16, A,
+                                     None, v, None) == code
+    st = state()
+    assert lib.lizard_attn_prefill_continue_v(A, A, A, A, A, 1.0, 128, 4, A, ctypes.byref(st), v, None) == code
+    assert lib.lizard_attn_decode_step_v(A, A, A, A, A, 1.0, 4, A, ctypes.byref(st), v, None) == code
+    assert lib.lizard_attn_backward_v(A, A, A, A, A, 1.0, 2, 4, 128, 128, 128, 64, 4, LA.LIZARD_BF16, A, A, A, A, A,
+                                      A, A, v, None) == code
+
+
+def test_valid_variant_on_empty_calls_launches_nothing(lib):
+    v = variant(alpha_h=A, Hkv=2)
+    assert lib.lizard_attn_prefill_v(A, A, A, A, A, 1.0, 0, 4, 128, 128, 128, 64, 4, LA.LIZARD_BF16, A,
+                                     None, v, None) == OK
+    assert lib.lizard_attn_prefill_continue_v(None, None, None, None, A, 1.0, 0, 4, None,
+                                              ctypes.byref(state()), v, None) == OK
