@@ -141,3 +141,32 @@ def test_llama3_8b_full_size_sampled_heads():
         r_s = torch.stack([r[name][0, 0] for r in refs])
         err = rel_l2(g_s, r_s)
         assert err <= TOL[torch.bfloat16], f"{name}: rel L2 {err:.3e}"
+
+
+def test_decay_stress_full_size_sampled_heads():
+    """B2 H32 L8192 d128 bf16, g ~ N(0, 2), w128 m8 alpha 0.5 (the exact
+    CUDA-core path: w > 65) in one launch; oracle on 3 sampled heads."""
+    wl = WORKLOADS["decay_stress"]
+    inp = prefill_inputs(wl)
+    gen = torch.Generator().manual_seed(98)
+    inp["dy"] = torch.randn(wl.B, wl.H, wl.L, wl.dv, generator=gen).to(inp["q"].dtype)
+    dq, dk, dv, dg, _, _ = _gpu_backward(inp, wl.w)
+    units = [(0, 3), (1, 0), (1, 30)]
+    import threading
+    refs = [None] * len(units)
+
+    def run(i, b, h):
+        sl = {n: inp[n][b, h][None, None] for n in ("q", "k", "v", "g", "dy")}
+        refs[i] = O.backward(sl["q"], sl["k"], sl["v"], sl["g"], inp["mu"][h:h + 1], wl.alpha, wl.w,
+                             sl["dy"].double(), threads=1)
+
+    ths = [threading.Thread(target=run, args=(i, b, h)) for i, (b, h) in enumerate(units)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg)):
+        g_s = torch.stack([got[b, h] for (b, h) in units])
+        r_s = torch.stack([r[name][0, 0] for r in refs])
+        err = rel_l2(g_s, r_s)
+        assert err <= TOL[torch.bfloat16], f"{name}: rel L2 {err:.3e}"
