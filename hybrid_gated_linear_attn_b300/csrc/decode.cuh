@@ -37,6 +37,10 @@ struct DecodeArgs {
     int B, H, w, m;
     const float *alpha_h;  // per-head anchor weights (null: alpha)
     int group;             // query heads per key/value head (k, v are [B][H / group][D])
+    // Failure-detection testing: polls of the first wait before it gives up
+    // (negative: the normal limit).  The drain after a timeout always keeps
+    // the normal limit, so the CTA retires only once its copies have landed.
+    int first_wait_polls;
 };
 
 constexpr int DECODE_THREADS = 256;
@@ -204,7 +208,8 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
     //    the CTA records it and waits (bounded) once more for its copies
     //    before its shared memory is released.
     bool ok = false;
-    for (uint32_t i = 0; i < DECODE_WAIT_LIMIT && !ok; ++i) ok = dec_try_wait(bar, 0);
+    const uint32_t first_cap = a.first_wait_polls < 0 ? DECODE_WAIT_LIMIT : (uint32_t)a.first_wait_polls;
+    for (uint32_t i = 0; i < first_cap && !ok; ++i) ok = dec_try_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
             atomicExch(&g_device_error, DEV_TIMEOUT);

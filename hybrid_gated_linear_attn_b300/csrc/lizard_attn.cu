@@ -12,6 +12,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -298,9 +299,22 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
     return rc;
 }
 
-template <typename T, int D>
-static lizard_status launch_decode(const DecodeArgs &da, cudaStream_t s)
+// Failure-detection testing: LIZARD_DEBUG_DECODE_FIRST_WAIT_POLLS=n (read
+// once per process) makes every decode step give up its first wait after n
+// polls and report LIZARD_ERR_TIMEOUT; unset, the normal limit applies.
+static int decode_first_wait_polls()
 {
+    static const int polls = [] {
+        const char *e = std::getenv("LIZARD_DEBUG_DECODE_FIRST_WAIT_POLLS");
+        return e && *e ? std::atoi(e) : -1;
+    }();
+    return polls;
+}
+
+template <typename T, int D>
+static lizard_status launch_decode(DecodeArgs da, cudaStream_t s)
+{
+    da.first_wait_polls = decode_first_wait_polls();
     const DecodePlan plan = decode_plan<D>((int)sizeof(T), da.w, da.m);
     if (plan.total > DECODE_SMEM_MAX) return LIZARD_ERR_UNSUPPORTED;
     auto kern = decode_step_kernel<T, D>;
@@ -767,7 +781,7 @@ lizard_status lizard_attn_decode_step_v(const void *q, const void *k, const void
     if (m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
     if (st->B == 0) return LIZARD_OK;
     DecodeArgs da{q, k, v, g, meta_k, y, st->S, st->ring_k, st->ring_v, st->pos, alpha, st->B, st->H, st->w, m,
-                  alpha_h, group};
+                  alpha_h, group, -1};
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
         return st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s) : launch_decode<__nv_bfloat16, 64>(da, s);

@@ -303,6 +303,16 @@ LIZARD_API lizard_status lizard_attn_decode_step_v(const void *q, const void *k,
                                         lizard_stream_t stream);
 
 /*
+ * Failure detection is testable without a GPU fault: with the environment
+ * variable LIZARD_DEBUG_DECODE_FIRST_WAIT_POLLS=n set when a process first
+ * decodes, every decode step of that process gives up its first wait (for
+ * its input copies) after n polls, records a timeout and skips its work,
+ * still waiting, with the normal limit, for its copies before it retires.
+ * lizard_check_device_status then reports LIZARD_ERR_TIMEOUT and the
+ * context stays usable.  For testing only; unset, the normal limit applies.
+ */
+
+/*
  * lizard_check_device_status: synchronises `stream`, then reads and clears
  * the library's device error word.  LIZARD_ERR_TIMEOUT if a kernel since the
  * last check abandoned a bounded wait (its outputs are then undefined),

@@ -154,3 +154,52 @@ def test_long_context_prefill_then_decode_sampled_heads():
     err_dec = rel_l2(got_dec, y_ref[:, wl.L:])
     assert err_dec <= 1e-2, f"decode rows: rel L2 {err_dec:.3e}"
     assert int(st.pos.cpu()[0]) == wl.L + n
+
+
+_TIMEOUT_CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+from hybrid_gated_linear_attn_b300 import (LizardError, LizardState, lizard_attn_decode_step,
+                                           lizard_check_device_status, lizard_state_init)
+from hybrid_gated_linear_attn_b300 import lizard_attn as LA
+B, H, d, w = 2, 4, 128, 64
+st = LizardState(B, H, d, d, w, dtype=torch.bfloat16)
+lizard_state_init(st)
+x = torch.randn(B, H, d, dtype=torch.bfloat16, device="cuda")
+mu = torch.randn(H, 4, d, dtype=torch.bfloat16, device="cuda")
+lizard_attn_decode_step(x, x, x, x, mu, 1.0, st)
+try:
+    lizard_check_device_status()
+    print("NO_TIMEOUT")
+except LizardError as e:
+    print("STATUS", e.status)
+print("POS", st.pos.cpu().tolist())
+lizard_check_device_status()  # cleared
+print("SUM", float(torch.ones(1000, device="cuda").sum()))  # the context is still usable
+"""
+
+
+def test_forced_decode_timeout_is_reported_and_context_stays_usable(tmp_path):
+    """Failure detection without a GPU fault: with the first wait capped at 0
+    polls every decode CTA gives up at once, records the timeout, still
+    waits (normal limit) for its copies, and retires; the host reads
+    LIZARD_ERR_TIMEOUT and the process keeps using the GPU."""
+    import os
+    import subprocess
+    import sys
+    from hybrid_gated_linear_attn_b300 import lizard_attn as LA
+    from hybrid_gated_linear_attn_b300 import lizard_attn_decode_step, lizard_check_device_status
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, LIZARD_DEBUG_DECODE_FIRST_WAIT_POLLS="0")
+    out = subprocess.run([sys.executable, "-c", _TIMEOUT_CHILD, root], env=env, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert f"STATUS {LA.LIZARD_ERR_TIMEOUT}" in out.stdout, out.stdout
+    assert "POS [1, 1]" in out.stdout, out.stdout  # the position still advances: every CTA counted itself
+    assert "SUM 1000.0" in out.stdout, out.stdout
+    # this process (no variable) decodes normally
+    st = LizardState(1, 2, 128, 128, 64, dtype=torch.bfloat16)
+    lizard_state_init(st)
+    x = torch.randn(1, 2, 128, dtype=torch.bfloat16, device="cuda")
+    lizard_attn_decode_step(x, x, x, x, None, 1.0, st)
+    lizard_check_device_status()
