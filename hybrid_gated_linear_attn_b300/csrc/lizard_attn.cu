@@ -176,13 +176,13 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
 
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                          const CUtensorMap &tg, const ws::WsArgs &wa, int ctas, cudaStream_t s)
+                                          const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
     auto kern = ws::prefill_ws_kernel<NP>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<ctas, ws::THREADS, smem, s>>>(tq, tk, tv, tg, wa);
+    kern<<<ctas, ws::THREADS, smem, s>>>(tq, tk, tv, wa);
     return launch_status();
 }
 
@@ -293,8 +293,8 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
                   nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg,
                   pa.cont, seg0_state, hist, pa.alpha_h, pa.group};
     if (rc == LIZARD_OK)
-        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, tg, wa, units * nseg, s)
-                       : launch_prefill_ws_np<1>(tq, tk, tv, tg, wa, units * nseg, s);
+        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, wa, units * nseg, s)
+                       : launch_prefill_ws_np<1>(tq, tk, tv, wa, units * nseg, s);
     if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -798,5 +798,13 @@ lizard_status lizard_check_device_status(lizard_stream_t stream)
     if (word == DEV_OK) return LIZARD_OK;
     return word == DEV_BAD_POS ? LIZARD_ERR_INVALID_ARG : LIZARD_ERR_TIMEOUT;
 }
+
+#ifdef LIZARD_TRACE
+// Debug builds only: the clock trace of the warp-specialised prefill's CTA 0.
+__attribute__((visibility("default"))) int lizard_debug_trace(unsigned long long *out)
+{
+    return cudaMemcpyFromSymbol(out, ws::g_ws_trace, sizeof(ws::g_ws_trace)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 }  // extern "C"

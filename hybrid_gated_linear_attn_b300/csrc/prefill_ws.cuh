@@ -18,24 +18,33 @@
 //   A   [t, s]  = QR_t . KR_s,  QR = q 2^{b-r}, KR = k 2^{r-b}  tcgen05, M=64
 //   W   [t, s'] = alpha softmax-with-sinks(SC)[t, s'] + A[t, s] (s <= t)
 //   Y^T [j, t]  = S16 QR^T + V_band^T W^T                       tcgen05, M=128
-//                 (S16 = bf16(S^T diag(2^r)) in tensor memory: q 2^{b} S)
+//                 (S16 = bf16(S_{c-1}^T diag(2^r)) in tensor memory)
 //   S^T        <- S^T diag(2^{b_last}) + V^T KL,  KL = k 2^{b_last - b}
+//
+// The state is kept as Shat = S / F per key dim, F = 2^{b_last - r} of the
+// last chunk folded in, because then the state update takes the same key
+// operand as A:  KL = KR F, so  S_c / F_c = (S_{c-1} 2^r) + V^T KR  in the
+// Shat form.  Per chunk the state pass scales Shat by F_{c-1} 2^{r_c} (which
+// is also the scale of S16), and the final state is Shat F.  Only two
+// operand tiles per chunk, so they are double-buffered and the gate prep of
+// chunk c+1 runs while chunk c is in its softmax and output products.
 //
 // The factors of A have exponents within +-(half-chunk decay span); a chunk
 // whose half-span exceeds SPAN2_MAX (base 2) for some key dimension is
 // "unsafe": its A is computed exactly on the CUDA cores instead
-// (sum_i q k 2^{b_t - b_s}, exponent <= 0), and its QR uses r = 0.  So every
-// gate value is handled.
+// (sum_i q k 2^{b_t - b_s}, exponent <= 0), its QR uses r = 0, its key
+// operand is KL itself and its F is 1.  So every gate value is handled.
 //
-// Warp roles (19 warps):
-//   warp 0       TMA producer: g and q tiles, k/v tiles (ring of NP+2)
-//   warp 1       MMA issuer (one thread): scores, A and the state update
+// Warp roles (20 warps):
+//   warp 0       TMA producer: q, k, v tiles (k/v ring of NP+2); L2 prefetch of g
+//   warp 1       MMA issuer (one thread): scores SC and A
 //   warp 2       MMA issuer (one thread): the two output products
-//   warps 3-6    state pass (S^T decay, S16) and y epilogue; the final state
-//   warps 7-14   gate prep: log-sigmoid, prefix sums, QR / KR / KL operands
-//   warps 15-18  window softmax: W from SC and A
-// Two issuers keep the state chain (scores, A, state update) from queueing
-// behind the output products, which wait for the softmax.
+//   warp 3       MMA issuer (one thread): the state update
+//   warps 4-7    state pass (Shat scale, S16) and the y epilogue (one chunk
+//                behind); the final state
+//   warps 8-15   gate prep: log-sigmoid (g read into registers one chunk
+//                ahead), prefix sums, the QR / KR operands and scale vectors
+//   warps 16-19  window softmax: W from SC and A
 // Every hand-off is an mbarrier; every wait is bounded (a timeout records
 // DEV_TIMEOUT, drains the copies and products in flight, and returns).
 #pragma once
@@ -51,9 +60,9 @@ using namespace sm100;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NWARPS = 19;
+constexpr int NWARPS = 20;
 constexpr int THREADS = NWARPS * 32;
-constexpr int W_TMA = 0, W_MMA = 1, W_MMAY = 2, W_EPI = 3, W_PREP = 7, W_SOFT = 15;
+constexpr int W_TMA = 0, W_MMA = 1, W_MMAY = 2, W_MMAS = 3, W_EPI = 4, W_PREP = 8, W_SOFT = 16;
 constexpr int EPI_N = 128, PREP_N = 256, SOFT_N = 128;
 enum : int { NB_EPI = 1, NB_PREP = 2, NB_SOFT = 3, NB_EPI_R = 4, NB_PREP_R = 5, NB_SOFT_R = 6 };
 constexpr int META_ROWS = 16;
@@ -68,21 +77,19 @@ constexpr uint32_t KB_K = KROWS * 128;     // one 64-dim block of a key tile (80
 constexpr uint32_t KB_T = C * 128;         // one 64-dim block of a 64-row tile
 constexpr uint32_t SLOT = 2 * KB_K + 2 * KB_T;
 constexpr uint32_t SLOT_V = 2 * KB_K;      // v tile within a slot
+constexpr uint32_t OPB = 4 * KB_T;         // one operand buffer: QR tile, then KR tile
+constexpr int NVEC = 3;                    // per operand buffer: sig, tau, F (fp32 [128] each)
 template <int NP>
 struct Smem {
     static constexpr int NR = NP + 2;
     static constexpr uint32_t KV = 0;
     static constexpr uint32_t Q = KV + NR * SLOT;
-    static constexpr uint32_t G = Q + QS * 2 * KB_T;       // gate logits of one chunk
-    static constexpr uint32_t QR = G + 2 * KB_T;
-    static constexpr uint32_t KR = QR + 2 * KB_T;
-    static constexpr uint32_t KL = KR + 2 * KB_T;
-    static constexpr uint32_t W = KL + 2 * KB_T;           // KL and W: 32 KB of exact-A scratch
-    static constexpr uint32_t W_BYTES = (NP + 1) * KB_T > 2 * KB_T ? (NP + 1) * KB_T : 2 * KB_T;
-    static constexpr uint32_t VEC = W + W_BYTES;           // dec[2][128], er[2][128], tot[4][128] (fp32)
-    static constexpr uint32_t FLAG = VEC + (2 * 128 + 2 * 128 + 4 * 128) * 4;  // unsafe[2], abort
+    static constexpr uint32_t OP = Q + QS * 2 * KB_T;      // two operand buffers
+    static constexpr uint32_t W = OP + 2 * OPB;
+    static constexpr uint32_t VEC = W + (NP + 1) * KB_T;   // [2][NVEC][128], then tot[4][128] (fp32)
+    static constexpr uint32_t FLAG = VEC + (2 * NVEC * 128 + 4 * 128) * 4;  // unsafe[2], abort
     static constexpr uint32_t BAR = FLAG + 16;
-    static constexpr int NBAR = 2 * QS + 4 * NR + 17;
+    static constexpr int NBAR = 2 * QS + 4 * NR + 4 + 13;
     static constexpr uint32_t TSLOT = BAR + NBAR * 8;
     static constexpr uint32_t USED = TSLOT + 16;
     static constexpr uint32_t BYTES = USED + 1024;
@@ -126,28 +133,27 @@ struct WsArgs {
     int group;             // query heads per key/value head (tk, tv map B x H / group heads)
 };
 
+// Optional clock trace of CTA 0 (compiled with -DLIZARD_TRACE): one clock64
+// stamp per (chunk, event), read by lizard_debug_trace.
+#ifdef LIZARD_TRACE
+constexpr int TRACE_CHUNKS = 64, TRACE_EVENTS = 24;
+__device__ unsigned long long g_ws_trace[TRACE_CHUNKS][TRACE_EVENTS];
+#define LZ_TRACE(pc, ev)                                                              \
+    do {                                                                              \
+        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (pc) < TRACE_CHUNKS) g_ws_trace[(pc)][(ev)] = clock64(); \
+    } while (0)
+#else
+#define LZ_TRACE(pc, ev) \
+    do {                 \
+    } while (0)
+#endif
+
 // ---------------------------------------------------------------- helpers
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-// 2^x on the FMA pipe: x = n + f with f in [0, 1); 2^f by a degree-4
-// least-squares polynomial (relative error < 4e-6), 2^n by exponent
-// arithmetic.  Returns 0 below 2^-126.
-__device__ __forceinline__ float exp2_fma(float x)
-{
-    x = fmaxf(x, -127.f);
-    const float n = floorf(x);
-    const float f = x - n;
-    float p = 0.013683983f;
-    p = fmaf(p, f, 0.051717736f);
-    p = fmaf(p, f, 0.24162132f);
-    p = fmaf(p, f, 0.69296956f);
-    p = fmaf(p, f, 1.0000036f);
-    const int e = (int)n;
-    return e < -126 ? 0.f : __int_as_float(__float_as_int(p) + (e << 23));
 }
 // log2(sigmoid(g)) = min(g, 0) log2(e) - log2(1 + u),  u = 2^{-|g| log2(e)} in (0, 1];
 // log2(1 + u) = u P(u) with a degree-7 least-squares polynomial (absolute
@@ -203,6 +209,12 @@ __device__ __forceinline__ float lg2(float x)
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float rcp(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float2 log2_sigmoid2(float2 g)
 {
     const float ua = ex2(-fabsf(g.x) * LOG2E), ub = ex2(-fabsf(g.y) * LOG2E);
@@ -217,6 +229,25 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi)
     __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&r);
 }
+// Streaming 4-byte load (read once: no L1 allocation).
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// Per-warpgroup register budgets (setmaxnreg): the CTA launches with
+// 640 threads x 96 registers = 61440; the TMA / MMA warpgroup drops to 40 and
+// the gate-prep and softmax warpgroups rise to 112:
+// 40*128 + 96*128 + 112*256 + 112*128 = 60416 <= 61440.
+template <uint32_t N> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+constexpr uint32_t REG_IO = 40, REG_WIDE = 112;
 __device__ __forceinline__ uint32_t tlane(uint32_t quarter) { return (32u * quarter) << 16; }
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ bool named_bar_and(int id, int n, bool p)
@@ -226,6 +257,19 @@ __device__ __forceinline__ bool named_bar_and(int id, int n, bool p)
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
         "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)p), "r"(id), "r"(n)
@@ -253,9 +297,28 @@ __device__ __forceinline__ bool role_wait(bool leader_warp, int lane, int id, in
 // or when another role already gave up.
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int *abort_flag)
 {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(bar, use & 1u)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
+    const uint32_t a = smem_u32(bar), par = use & 1u;
+#pragma unroll 1
+    for (uint32_t i = 0; i < WAIT_LIMIT / 256u; ++i) {
+        uint32_t ok;
+        // up to 256 polls in one loop of the PTX itself (small code)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .u32 n;\n\t"
+            "mov.u32 n, 256;\n\t"
+            "LZ_POLL_%=:\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "@p bra.uni LZ_DONE_%=;\n\t"
+            "sub.u32 n, n, 1;\n\t"
+            "setp.ne.u32 p, n, 0;\n\t"
+            "@p bra.uni LZ_POLL_%=;\n\t"
+            "LZ_DONE_%=:\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(a), "r"(par)
+            : "memory");
+        // p is true on success; after 256 failed polls n = 0 and p is false
+        if (ok) return true;
+        if (*abort_flag) return false;
     }
     return false;
 }
@@ -263,7 +326,7 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int 
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const WsArgs a)
+                      const __grid_constant__ CUtensorMap tv, const WsArgs a)
 {
     using SM = Smem<NP>;
     using TM = Tmem<NP>;
@@ -272,23 +335,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float *dec_v = reinterpret_cast<float *>(sm + SM::VEC);   // [2][128] 2^{b_last}
-    float *er_v = dec_v + 256;                                  // [2][128] 2^{r}
-    float *tot = er_v + 256;                                    // [4][128] quarter totals
-    volatile int *unsafe_f = reinterpret_cast<volatile int *>(sm + SM::FLAG);  // [2]
+    // Scale vectors of operand buffer b: vec + b * NVEC * 128 -> sig (state
+    // pass: Shat scale), tau (S16 scale), F (the chunk's state factor).
+    float *vec = reinterpret_cast<float *>(sm + SM::VEC);
+    float *tot = vec + 2 * NVEC * 128;                          // [4][128] quarter totals
+    volatile int *unsafe_f = reinterpret_cast<volatile int *>(sm + SM::FLAG);  // [2], per operand buffer
     volatile int *abort_f = unsafe_f + 2;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::BAR);
     // k and v of a slot load and free separately: a key tile is free once
-    // the band scores that read it are done, a value tile only after the
-    // output products.
+    // the band scores that read it are done, a value tile after its state
+    // update and the output products (two arrivals).
     uint64_t *q_full = bars, *q_empty = bars + QS, *k_full = bars + 2 * QS, *k_empty = k_full + NR;
     uint64_t *v_full = k_empty + NR, *v_empty = v_full + NR;
-    uint64_t *g_full = v_empty + NR, *g_empty = g_full + 1;
-    uint64_t *prep_ready = g_empty + 1, *kr_free = prep_ready + 1, *qr_free = prep_ready + 2,
-             *kl_free = prep_ready + 3, *sc_full = prep_ready + 4, *a_full = prep_ready + 5,
-             *sc_free = prep_ready + 6, *w_full = prep_ready + 7, *w_free = prep_ready + 8,
-             *s_ready = prep_ready + 9, *st_done = prep_ready + 10, *y_full = prep_ready + 11,
-             *y_free = prep_ready + 12, *drain = prep_ready + 13, *drain_y = prep_ready + 14;
+    uint64_t *op_full = v_empty + NR, *op_free = op_full + 2;   // per operand buffer
+    uint64_t *sc_full = op_free + 2, *a_full = sc_full + 1, *sc_free = sc_full + 2, *w_full = sc_full + 3,
+             *w_free = sc_full + 4, *s_ready = sc_full + 5, *st_done = sc_full + 6, *s16_free = sc_full + 7,
+             *y_full = sc_full + 8, *y_free = sc_full + 9, *drain = sc_full + 10, *drain_y = sc_full + 11,
+             *drain_s = sc_full + 12;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM::TSLOT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -312,17 +375,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (tid == 0) {
         for (int i = 0; i < QS; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 2);
+            mbar_init(&q_empty[i], 2);   // scores issued + prep read q
         }
         for (int i = 0; i < NR; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], 2);   // state update + output products
         }
-        mbar_init(g_full, 1);
-        mbar_init(g_empty, 1);
-        for (int i = 0; i < 15; ++i) mbar_init(&prep_ready[i], i == 5 ? 2 : 1);  // a_full: MMA + prep
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&op_full[i], 1);
+            mbar_init(&op_free[i], 3);   // A, the readout, the state update
+        }
+        for (int i = 0; i < 13; ++i) mbar_init(&sc_full[i], 1);
         unsafe_f[0] = 0;
         unsafe_f[1] = 0;
         *abort_f = 0;
@@ -330,7 +395,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
-        prefetch_tmap(&tg);
         *p0_slot = a.cont ? take_start_position(a.pos + unit / a.H, a.H * nseg, L) : 0;
     }
     if (a.cont) __syncthreads();  // p0
@@ -380,10 +444,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         atomicExch(&g_device_error, DEV_TIMEOUT);
     };
 
+
     if (warp == W_TMA) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {}, g_issued = 0;
+            uint32_t k_issued[NR] = {}, v_issued[NR] = {}, q_issued[QS] = {};
+            // The gate logits go straight to registers in the prep role; a
+            // bulk prefetch two chunks ahead keeps them in L2.
+            auto prefetch_g = [&](int c) {
+                const int n = min(C, L - c * C);
+                prefetch_l2(a.g + ((size_t)unit * L + (size_t)c * C) * D, (uint32_t)n * D * 2u);
+            };
+            for (int c = c_begin; c < min(c_end, c_begin + 2); ++c) prefetch_g(c);
             // keys and values of the band chunks before this segment; the
             // window history (chunk -1) is in place since the set-up
             for (int c = c_lo; c < c_begin; ++c) {
@@ -405,11 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             for (int c = c_begin; c < c_end && !failed; ++c) {
                 const int pc = c - c_begin, r = c - c_lo;
-                if (pc >= 1 && !bwait(g_empty, pc - 1, abort_f)) { give_up(); break; }
-                mbar_arrive_expect_tx(g_full, 2 * KB_T);
-                tma_load_3d(sm + SM::G, &tg, g_full, 0, c * C, unit);
-                tma_load_3d(sm + SM::G + KB_T, &tg, g_full, 64, c * C, unit);
-                ++g_issued;
+                if (c + 2 < c_end) prefetch_g(c + 2);
                 const int s = r % NR;
                 uint8_t *base = sm + SM::KV + s * SLOT;
                 if (r >= NR && !bwait(&k_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
@@ -417,17 +485,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_3d(base, &tk, &k_full[s], 0, c * C, kvu);
                 tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, kvu);
                 ++k_issued[s];
+                LZ_TRACE(pc, 15);
                 const int qs = pc % QS;
                 if (pc >= QS && !bwait(&q_empty[qs], pc / QS - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&q_full[qs], 2 * KB_T);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T, &tq, &q_full[qs], 0, c * C, unit);
                 tma_load_3d(sm + SM::Q + qs * 2 * KB_T + KB_T, &tq, &q_full[qs], 64, c * C, unit);
                 ++q_issued[qs];
+                LZ_TRACE(pc, 16);
                 if (r >= NR && !bwait(&v_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
                 mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
                 tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, kvu);
                 tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, kvu);
                 ++v_issued[s];
+                LZ_TRACE(pc, 17);
             }
             // Drain: every copy issued has landed before shared memory is released.
             for (int s = 0; s < NR; ++s) {
@@ -436,19 +507,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             for (int s = 0; s < QS; ++s)
                 if (q_issued[s]) bwait(&q_full[s], q_issued[s] - 1, abort_f);
-            if (g_issued) bwait(g_full, g_issued - 1, abort_f);
         }
         __syncwarp();
     } else if (warp == W_MMA) {
-        // ------------------------------------------------------ MMA issuer: scores, A, state
+        // ------------------------------------------------------ MMA issuer: scores SC and A
         if (lane == 0) {
             const uint32_t id_sc_prev = instr_desc(64, 64, FMT_BF16, 0, 0);
             const uint32_t id_sc_cur = instr_desc(64, 64 + META_ROWS, FMT_BF16, 0, 0);
             const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
-            const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
             for (int c = c_begin; c < c_end; ++c) {
                 const int pc = c - c_begin, r = c - c_lo;
-                const int s = r % NR, qs = pc % QS;
+                const int s = r % NR, qs = pc % QS, b = pc & 1;
                 const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
                 if ((pc == 0 && c_lo < c_begin && !bwait(&k_full[0], 0, abort_f)) ||
                     !bwait(&k_full[s], r / NR, abort_f) || !bwait(&q_full[qs], pc / QS, abort_f) ||
@@ -468,37 +537,57 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mma_commit(sc_full);
                 mma_commit(&q_empty[qs]);
+                LZ_TRACE(pc, 3);
                 // intra-chunk decayed scores
-                if (!bwait(prep_ready, pc, abort_f)) { give_up(); break; }
+                if (!bwait(&op_full[b], pc >> 1, abort_f)) { give_up(); break; }
                 tc_fence_after();
-                if (!unsafe_f[pc & 1]) {
+                if (!unsafe_f[b]) {
+                    const uint32_t ob = sb + SM::OP + b * OPB;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ss(tmem + TM::A, smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
-                                    smem_desc(sb + SM::KR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_a, kk > 0);
+                        mma_bf16_ss(tmem + TM::A, smem_desc(ob + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
+                                    smem_desc(ob + 2 * KB_T + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_a,
+                                    kk > 0);
+                    mma_commit(a_full);
+                } else {
+                    mbar_arrive(a_full);  // exact A, stored by the prep role before op_full
                 }
-                mma_commit(a_full);
-                mma_commit(kr_free);
+                LZ_TRACE(pc, 4);
                 // The key tile of chunk c - NP has no reader left: the last
                 // band scores that use it were issued above, and its raw keys
-                // were read by the prep of chunk c - NP (done: prep_ready).
+                // were read by the prep of chunk c - NP (done: op_full).
                 if (c - NP >= c_lo) mma_commit(&k_empty[(c - NP - c_lo) % NR]);
-                // S^T += V^T KL (S^T decayed by the state pass)
-                if (!bwait(s_ready, pc, abort_f) || !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
-                tc_fence_after();
-                {
-                    const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
-                                    smem_desc(sb + SM::KL + kk * 2048, KB_T, 1024), id_st, 1u);
-                }
-                mma_commit(st_done);
-                mma_commit(kl_free);
+                mma_commit(&op_free[b]);
             }
             // Drain: every product issued has completed before tensor memory is released.
             mma_commit(drain);
             bwait(drain, 0, abort_f);
+        }
+        __syncwarp();
+    } else if (warp == W_MMAS) {
+        // ------------------------------------------------------ MMA issuer: state update
+        if (lane == 0) {
+            const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
+            // band chunks before the segment get no state update here
+            for (int c = c_lo; c < c_begin; ++c) mbar_arrive(&v_empty[(c - c_lo) % NR]);
+            for (int c = c_begin; c < c_end; ++c) {
+                const int pc = c - c_begin, r = c - c_lo, s = r % NR, b = pc & 1;
+                if (!bwait(s_ready, pc, abort_f) || !bwait(&op_full[b], pc >> 1, abort_f) ||
+                    !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
+                tc_fence_after();
+                // Shat^T += V^T K, K = KR (KL for an unsafe chunk)
+                const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V, kb = sb + SM::OP + b * OPB + 2 * KB_T;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
+                                smem_desc(kb + kk * 2048, KB_T, 1024), id_st, 1u);
+                mma_commit(st_done);
+                mma_commit(&op_free[b]);
+                mma_commit(&v_empty[s]);
+                LZ_TRACE(pc, 5);
+            }
+            mma_commit(drain_s);
+            bwait(drain_s, 0, abort_f);
         }
         __syncwarp();
     } else if (warp == W_MMAY) {
@@ -507,20 +596,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t id_y1 = instr_desc(128, 64, FMT_BF16, 0, 0);
             const uint32_t id_y2 = instr_desc(128, 64, FMT_BF16, 1, 0);
             for (int c = c_begin; c < c_end; ++c) {
-                const int pc = c - c_begin, r = c - c_lo;
+                const int pc = c - c_begin, r = c - c_lo, b = pc & 1;
                 // y^T = S16 QR^T (inter-chunk readout)
-                if (!bwait(prep_ready, pc, abort_f) || !bwait(s_ready, pc, abort_f) ||
+                if (!bwait(&op_full[b], pc >> 1, abort_f) || !bwait(s_ready, pc, abort_f) ||
                     (pc >= 1 && !bwait(y_free, pc - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
+                const uint32_t ob = sb + SM::OP + b * OPB;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8,
-                                smem_desc(sb + SM::QR + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
-                mma_commit(qr_free);
+                                smem_desc(ob + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
+                mma_commit(s16_free);
+                mma_commit(&op_free[b]);
+                LZ_TRACE(pc, 6);
                 // y^T += V_band^T W^T
                 if (!bwait(w_full, pc, abort_f) || !bwait(&v_full[r % NR], r / NR, abort_f) ||
-                    (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f)) ||
-                    (NP == 0 && !bwait(st_done, pc, abort_f))) { give_up(); break; }
+                    (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f))) { give_up(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j <= NP; ++j) {
@@ -534,9 +625,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mma_commit(y_full);
                 mma_commit(w_free);
-                // The value tile of chunk c - NP has no reader left: its state
-                // update (issued before A_c, which the softmax waited for;
-                // for NP = 0 st_done above) and these products.
+                LZ_TRACE(pc, 7);
+                // The value tile of chunk c - NP has no reader left among the
+                // output products (its state update commits separately).
                 if (c - NP >= c_lo) mma_commit(&v_empty[(c - NP - c_lo) % NR]);
             }
             mma_commit(drain_y);
@@ -564,48 +655,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_wait_st();
         }
         const int et = tid - W_EPI * 32;
-        for (int c = c_begin; c < c_end; ++c) {
-            const int pc = c - c_begin;
-            const int c0 = c * C, n = min(C, L - c0);
-            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] {
-                    return (pc == 0 || (bwait(st_done, pc - 1, abort_f) && bwait(qr_free, pc - 1, abort_f))) &&
-                           bwait(prep_ready, pc, abort_f);
-                })) { give_up(); break; }
+        // y rows of chunk c_begin + py: read the accumulator, store bf16.
+        auto epilogue = [&](int py) -> bool {
+            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] { return bwait(y_full, py, abort_f); }))
+                return false;
+            LZ_TRACE(py, 10);
             tc_fence_after();
-            const float *dv = dec_v + (pc & 1) * 128, *ev = er_v + (pc & 1) * 128;
-#pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
-                uint32_t r0[16], r1[16];
-                tmem_ld16(tl + T_S + cb, r0);
-                tmem_ld16(tl + T_S + cb + 16, r1);
-                tmem_wait_ld();
-                uint32_t p16[16];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p16[e] = f2_to_bf2(__uint_as_float(r0[2 * e]) * ev[cb + 2 * e],
-                                       __uint_as_float(r0[2 * e + 1]) * ev[cb + 2 * e + 1]);
-                    p16[8 + e] = f2_to_bf2(__uint_as_float(r1[2 * e]) * ev[cb + 16 + 2 * e],
-                                           __uint_as_float(r1[2 * e + 1]) * ev[cb + 16 + 2 * e + 1]);
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    r0[e] = __float_as_uint(__uint_as_float(r0[e]) * dv[cb + e]);
-                    r1[e] = __float_as_uint(__uint_as_float(r1[e]) * dv[cb + 16 + e]);
-                }
-                tmem_st16(tl + T_S16 + cb / 2, p16);
-                tmem_st16(tl + T_S + cb, r0);
-                tmem_st16(tl + T_S + cb + 16, r1);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            named_bar(NB_EPI, EPI_N);
-            if (et == 0) mbar_arrive(s_ready);
-            // epilogue: y rows of this chunk
-            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] { return bwait(y_full, pc, abort_f); })) {
-                give_up();
-                break;
-            }
-            tc_fence_after();
+            const int c0 = (c_begin + py) * C, n = min(C, L - c0);
             __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
 #pragma unroll 1
             for (int cc = 0; cc < C; cc += 16) {
@@ -619,12 +675,77 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             named_bar(NB_EPI, EPI_N);
             if (et == 0) mbar_arrive(y_free);
+            LZ_TRACE(py, 11);
+            return true;
+        };
+        for (int c = c_begin; c < c_end; ++c) {
+            const int pc = c - c_begin, b = pc & 1;
+            if (!role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N, [&] {
+                    return (pc == 0 || (bwait(st_done, pc - 1, abort_f) && bwait(s16_free, pc - 1, abort_f))) &&
+                           bwait(&op_full[b], pc >> 1, abort_f);
+                })) { give_up(); break; }
+            LZ_TRACE(pc, 8);
+            tc_fence_after();
+            const float *sg = vec + b * NVEC * 128, *tv = sg + 128;
+            // Shat <- Shat sig and S16 = bf16(Shat tau); sig = tau except in
+            // an unsafe chunk, so one product serves both.
+            const bool one = !unsafe_f[b];
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tl + T_S + cb, r0);
+                tmem_ld16(tl + T_S + cb + 16, r1);
+                tmem_wait_ld();
+                uint32_t p16[16];
+                if (one) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 sv = *reinterpret_cast<const float2 *>(sg + cb + e);
+                        const float2 sw = *reinterpret_cast<const float2 *>(sg + cb + 16 + e);
+                        const float2 a0 = mul2(make_float2(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1])), sv);
+                        const float2 a1 = mul2(make_float2(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1])), sw);
+                        r0[e] = __float_as_uint(a0.x);
+                        r0[e + 1] = __float_as_uint(a0.y);
+                        r1[e] = __float_as_uint(a1.x);
+                        r1[e + 1] = __float_as_uint(a1.y);
+                        p16[e / 2] = f2_to_bf2(a0.x, a0.y);
+                        p16[8 + e / 2] = f2_to_bf2(a1.x, a1.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        p16[e] = f2_to_bf2(__uint_as_float(r0[2 * e]) * tv[cb + 2 * e],
+                                           __uint_as_float(r0[2 * e + 1]) * tv[cb + 2 * e + 1]);
+                        p16[8 + e] = f2_to_bf2(__uint_as_float(r1[2 * e]) * tv[cb + 16 + 2 * e],
+                                               __uint_as_float(r1[2 * e + 1]) * tv[cb + 16 + 2 * e + 1]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        r0[e] = __float_as_uint(__uint_as_float(r0[e]) * sg[cb + e]);
+                        r1[e] = __float_as_uint(__uint_as_float(r1[e]) * sg[cb + 16 + e]);
+                    }
+                }
+                tmem_st16(tl + T_S16 + cb / 2, p16);
+                tmem_st16(tl + T_S + cb, r0);
+                tmem_st16(tl + T_S + cb + 16, r1);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar(NB_EPI, EPI_N);
+            if (et == 0) mbar_arrive(s_ready);
+            LZ_TRACE(pc, 9);
+            // epilogue of the previous chunk (its readout waited for this
+            // role's previous iteration only)
+            if (pc >= 1 && !epilogue(pc - 1)) { give_up(); break; }
         }
-        // Final state S (row i = key dim): S^T[j][i] -> S_out[i][j].
+        if (!failed && c_end > c_begin && !epilogue(c_end - c_begin - 1)) give_up();
+        // Final state S = Shat F (row i = key dim): Shat^T[j][i] F[i] -> S_out[i][j].
         if (!failed && a.S_out && last_seg) {
+            const int nch = c_end - c_begin;
             if (role_wait(warp == W_EPI, lane, NB_EPI_R, EPI_N,
-                          [&] { return c_end == c_begin || bwait(st_done, c_end - c_begin - 1, abort_f); })) {
+                          [&] { return nch == 0 || bwait(st_done, nch - 1, abort_f); })) {
                 tc_fence_after();
+                const float *Fv = vec + ((nch - 1) & 1) * NVEC * 128 + 256;
                 float *So = a.S_out + (size_t)unit * D * D + j;
 #pragma unroll 1
                 for (int cc = 0; cc < D; cc += 16) {
@@ -632,7 +753,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld16(tl + T_S + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) So[(size_t)(cc + e) * D] = __uint_as_float(r[e]);
+                    for (int e = 0; e < 16; ++e)
+                        So[(size_t)(cc + e) * D] = nch == 0 ? __uint_as_float(r[e]) : __uint_as_float(r[e]) * Fv[cc + e];
                 }
             } else {
                 give_up();
@@ -640,94 +762,133 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= W_PREP && warp < W_PREP + 8) {
         // ------------------------------------------------------ gate prep
+        // Product form: per element iv = 1 / sigmoid(g) = 1 + 2^{-g log2 e}
+        // (= 2^{-lambda}), so the operand scales are running products of iv
+        // (no log or exponential per element beyond the one ex2).  Tokens
+        // past the end read g = +inf: iv = 1, no decay.
         const int tp = tid - W_PREP * 32;
         const int p = tp & 63, hq = tp >> 6;       // key dims 2p, 2p+1; tokens 16 hq .. 16 hq + 15
         const uint32_t kblk = (p / 32), kbyte = (p % 32) * 4;
+        // Gate logits of the chunk being prepared, loaded one chunk ahead.
+        const __nv_bfloat16 *gsrc = a.g + (size_t)unit * L * D + 2 * p;
+        uint32_t gr[16];
+        auto load_g = [&](int c) {
+            const int t0 = c * C + 16 * hq;
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt)
+                gr[tt] = t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
+        };
+        if (c_begin < c_end) load_g(c_begin);
+        float2 Fp = make_float2(1.f, 1.f);         // F of the previous chunk (1: Shat = S at the start)
         for (int c = c_begin; c < c_end; ++c) {
             const int pc = c - c_begin, r = c - c_lo;
-            const int s = r % NR, qs = pc % QS;
-            const int n = min(C, L - c * C);
-            if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] { return bwait(g_full, pc, abort_f); })) {
-                give_up();
-                break;
-            }
-            // 1. log-gates and the quarter's prefix sums (base 2); tokens past
-            //    the end of the sequence get no decay.
-            float2 cs[16];
+            const int s = r % NR, qs = pc % QS, b = pc & 1;
+            LZ_TRACE(pc, 0);
+            // 1. iv per element and the quarter's product
+            float2 iv[16];
             {
-                float2 run = make_float2(0.f, 0.f);
+                float2 prod = make_float2(1.f, 1.f);
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) {
-                    const int t = 16 * hq + tt;
-                    const float2 gg = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + SM::G + kblk * KB_T +
-                                                                                   sw128_offset(t, kbyte)));
-                    const float2 l = log2_sigmoid2(gg);
-                    if (t < n) run = add2(run, l);
-                    cs[tt] = run;
+                    const float2 g2 = bf2_to_f2(gr[tt]);
+                    iv[tt] = make_float2(1.f + ex2(g2.x * -LOG2E), 1.f + ex2(g2.y * -LOG2E));
+                    prod = mul2(prod, iv[tt]);
                 }
-                tot[hq * 128 + 2 * p] = run.x;
-                tot[hq * 128 + 2 * p + 1] = run.y;
+                LZ_TRACE(pc, 18);
+                if (c + 1 < c_end) load_g(c + 1);
+                *reinterpret_cast<float2 *>(tot + hq * 128 + 2 * p) = prod;
             }
+            LZ_TRACE(pc, 19);
             named_bar(NB_PREP, PREP_N);
-            if (tp == 0) mbar_arrive(g_empty);  // every prep thread has read this chunk's g
-            // 2. chunk offsets: r = b at token 31, b_last = b at token 63
+            LZ_TRACE(pc, 20);
+            // 2. quarter products: 2^{-r} = T0 T1, 2^{-(b_last - r)} = T2 T3
             float2 T[4];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) T[qq] = make_float2(tot[qq * 128 + 2 * p], tot[qq * 128 + 2 * p + 1]);
-            const float2 half0 = make_float2(T[0].x + T[1].x, T[0].y + T[1].y);
-            const float2 half1 = make_float2(T[2].x + T[3].x, T[2].y + T[3].y);
-            float2 pre = make_float2(0.f, 0.f);  // b at the end of the previous quarter
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-                if (qq < hq) { pre.x += T[qq].x; pre.y += T[qq].y; }
-            if (fmaxf(fmaxf(-half0.x, -half1.x), fmaxf(-half0.y, -half1.y)) > SPAN2_MAX) unsafe_f[pc & 1] = 1;
+            for (int qq = 0; qq < 4; ++qq) T[qq] = *reinterpret_cast<const float2 *>(tot + qq * 128 + 2 * p);
+            const float2 h0 = mul2(T[0], T[1]), h1 = mul2(T[2], T[3]);
+            constexpr float SPAN_MAX = 1.2676506e30f;  // 2^SPAN2_MAX
+            const bool wide = !(fmaxf(fmaxf(h0.x, h0.y), fmaxf(h1.x, h1.y)) <= SPAN_MAX);
             if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                    return bwait(&k_full[s], r / NR, abort_f) && bwait(&q_full[qs], pc / QS, abort_f);
+                    return bwait(&k_full[s], r / NR, abort_f) && bwait(&q_full[qs], pc / QS, abort_f) &&
+                           (pc < 2 || bwait(&op_free[b], (pc >> 1) - 1, abort_f));
                 })) { give_up(); break; }
-            const bool unsafe = unsafe_f[pc & 1] != 0;
+            LZ_TRACE(pc, 21);
+            // every prep thread has read tot: the next step may overwrite it
+            const bool unsafe = named_bar_or(NB_PREP, PREP_N, wide);
+            LZ_TRACE(pc, 1);
             const uint8_t *kraw = sm + SM::KV + s * SLOT + kblk * KB_K;
             const uint8_t *qraw = sm + SM::Q + qs * 2 * KB_T + kblk * KB_T;
-            const float2 blast = make_float2(half0.x + half1.x, half0.y + half1.y);
+            uint8_t *qr_t = sm + SM::OP + b * OPB + kblk * KB_T, *kr_t = qr_t + 2 * KB_T;
+            float *vb = vec + b * NVEC * 128;
             if (!unsafe) {
-                // b_t - r for this thread's tokens: cs + (pre - half0)
-                const float2 o = make_float2(pre.x - half0.x, pre.y - half0.y);
-                const float2 F = make_float2(ex2(half1.x), ex2(half1.y));  // 2^{b_last - r}
-                if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                        return pc == 0 || (bwait(kr_free, pc - 1, abort_f) && bwait(qr_free, pc - 1, abort_f) &&
-                                          bwait(kl_free, pc - 1, abort_f));
-                    })) { give_up(); break; }
-                uint8_t *kr_t = sm + SM::KR + kblk * KB_T, *qr_t = sm + SM::QR + kblk * KB_T;
-                uint8_t *kl_t = sm + SM::KL + kblk * KB_T;
-#pragma unroll
-                for (int tt = 0; tt < 16; ++tt) {
+                auto emit = [&](int tt, float2 qs2, float2 ks2) {
                     const uint32_t off = sw128_offset(16 * hq + tt, kbyte);
                     const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
                     const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
-                    const float2 e = add2(cs[tt], o);
-                    const float2 kr = mul2(kv, make_float2(ex2(-e.x), ex2(-e.y)));
-                    const float2 qr = mul2(qv, make_float2(ex2(e.x), ex2(e.y)));
-                    const float2 kl = mul2(kr, F);
+                    const float2 kr = mul2(kv, ks2), qr = mul2(qv, qs2);
                     *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
                     *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
-                    *reinterpret_cast<uint32_t *>(kl_t + off) = f2_to_bf2(kl.x, kl.y);
+                };
+                // Z_t = 2^{r - b_t}: a running product of iv from the start
+                // of the thread's half, times 2^r in the first half
+                // (2^{r - b_t} = 2^r prod_{0..t} iv there).  KR = k Z,
+                // QR = q / Z; every factor lies in [2^-SPAN2_MAX, 2^SPAN2_MAX].
+                const float2 er = make_float2(rcp(h0.x), rcp(h0.y));     // 2^r
+                float2 R = hq == 0 ? er : hq == 1 ? mul2(er, T[0]) : hq == 2 ? make_float2(1.f, 1.f) : T[2];
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    R = mul2(R, iv[tt]);
+                    const uint32_t off = sw128_offset(16 * hq + tt, kbyte);
+                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
+                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
+                    const float2 kr = mul2(kv, R), qr = mul2(qv, make_float2(rcp(R.x), rcp(R.y)));
+                    *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
+                    *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
                 }
+                const float2 F = make_float2(rcp(h1.x), rcp(h1.y));       // 2^{b_last - r}
+                const float2 sc = mul2(Fp, er);                              // F_{c-1} 2^r
                 if (hq == 0) {
-                    er_v[(pc & 1) * 128 + 2 * p] = ex2(half0.x);
-                    er_v[(pc & 1) * 128 + 2 * p + 1] = ex2(half0.y);
+                    *reinterpret_cast<float2 *>(vb + 2 * p) = sc;
+                    *reinterpret_cast<float2 *>(vb + 128 + 2 * p) = sc;
+                    *reinterpret_cast<float2 *>(vb + 256 + 2 * p) = F;
                 }
+                Fp = F;
             } else {
-                // Exact intra-chunk scores on the CUDA cores.  Scratch: the
-                // KL and W tiles hold b (fp32, [64][128]) meanwhile.
+                // Exact intra-chunk scores on the CUDA cores, in log space:
+                // b_t = sum log2 sigmoid(g) from this chunk's logits (read
+                // again: the registers hold the next chunk's by now).
+                // Scratch: the other operand buffer holds b (fp32, [64][128])
+                // meanwhile; its chunk's products and the previous softmax
+                // (which read the A columns) are done.
+                float2 cs[16];
+                {
+                    float2 run = make_float2(0.f, 0.f);
+                    const int t0 = c * C + 16 * hq;
+#pragma unroll
+                    for (int tt = 0; tt < 16; ++tt) {
+                        const uint32_t gv =
+                            t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
+                        run = add2(run, log2_sigmoid2(bf2_to_f2(gv)));
+                        cs[tt] = run;
+                    }
+                    *reinterpret_cast<float2 *>(tot + hq * 128 + 2 * p) = run;
+                }
                 if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
-                        return pc == 0 || (bwait(kl_free, pc - 1, abort_f) && bwait(w_free, pc - 1, abort_f) &&
-                                          bwait(sc_free, pc - 1, abort_f) && bwait(kr_free, pc - 1, abort_f) &&
-                                          bwait(qr_free, pc - 1, abort_f));
+                        return pc == 0 ||
+                               (bwait(&op_free[b ^ 1], (pc - 1) >> 1, abort_f) && bwait(sc_free, pc - 1, abort_f));
                     })) { give_up(); break; }
-                float *bz = reinterpret_cast<float *>(sm + SM::KL);
+                float2 Tl[4];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) Tl[qq] = *reinterpret_cast<const float2 *>(tot + qq * 128 + 2 * p);
+                float2 pre = make_float2(0.f, 0.f);  // b at the end of the previous quarter
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qq < hq) pre = add2(pre, Tl[qq]);
+                const float2 blast = add2(add2(Tl[0], Tl[1]), add2(Tl[2], Tl[3]));
+                float *bz = reinterpret_cast<float *>(sm + SM::OP + (b ^ 1) * OPB);
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt)
-                    *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) =
-                        make_float2(cs[tt].x + pre.x, cs[tt].y + pre.y);
+                    *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) = add2(cs[tt], pre);
                 named_bar(NB_PREP, PREP_N);
                 {
                     const int quarter = warp & 3, li = ((warp - W_PREP) >> 2) * 32 + lane;
@@ -751,44 +912,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                         }
                     }
-                    uint32_t r[16];
+                    uint32_t rr[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(acc[e]);
-                    tmem_st16_x2<16>(tmem + tlane(quarter) + TM::A + 32 * ((warp - W_PREP) >> 2), r);
+                    for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(acc[e]);
+                    tmem_st16_x2<16>(tmem + tlane(quarter) + TM::A + 32 * ((warp - W_PREP) >> 2), rr);
                     tmem_wait_st();
                 }
                 tc_fence_before();
                 named_bar(NB_PREP, PREP_N);
-                if (tp == 0) mbar_arrive(a_full);
-                // QR with r = 0 (exponents <= 0), KL exact.
+                // QR with r = 0 (exponents <= 0); the key operand is KL, F = 1.
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) {
                     const int t = 16 * hq + tt;
-                    const float2 bt = make_float2(cs[tt].x + pre.x, cs[tt].y + pre.y);
-                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + sw128_offset(t, kbyte)));
-                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + sw128_offset(t, kbyte)));
-                    *reinterpret_cast<uint32_t *>(sm + SM::QR + kblk * KB_T + sw128_offset(t, kbyte)) =
-                        f2_to_bf2(qv.x * ex2(bt.x), qv.y * ex2(bt.y));
-                    *reinterpret_cast<uint32_t *>(sm + SM::KL + kblk * KB_T + sw128_offset(t, kbyte)) =
+                    const uint32_t off = sw128_offset(t, kbyte);
+                    const float2 bt = *reinterpret_cast<const float2 *>(bz + t * D + 2 * p);
+                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
+                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
+                    *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qv.x * ex2(bt.x), qv.y * ex2(bt.y));
+                    *reinterpret_cast<uint32_t *>(kr_t + off) =
                         f2_to_bf2(kv.x * ex2(blast.x - bt.x), kv.y * ex2(blast.y - bt.y));
                 }
                 if (hq == 0) {
-                    er_v[(pc & 1) * 128 + 2 * p] = 1.f;
-                    er_v[(pc & 1) * 128 + 2 * p + 1] = 1.f;
+                    *reinterpret_cast<float2 *>(vb + 2 * p) = make_float2(Fp.x * ex2(blast.x), Fp.y * ex2(blast.y));
+                    *reinterpret_cast<float2 *>(vb + 128 + 2 * p) = Fp;
+                    *reinterpret_cast<float2 *>(vb + 256 + 2 * p) = make_float2(1.f, 1.f);
                 }
-            }
-            if (hq == 0) {
-                dec_v[(pc & 1) * 128 + 2 * p] = ex2(blast.x);
-                dec_v[(pc & 1) * 128 + 2 * p + 1] = ex2(blast.y);
+                Fp = make_float2(1.f, 1.f);
             }
             fence_proxy_async_smem();
             named_bar(NB_PREP, PREP_N);
             if (tp == 0) {
-                unsafe_f[(pc + 1) & 1] = 0;  // the MMA issuer read it for chunk c - 1 before state_{c-1}
-                mbar_arrive(prep_ready);
-                if (!unsafe) mbar_arrive(a_full);
+                unsafe_f[b] = unsafe ? 1 : 0;
+                mbar_arrive(&op_full[b]);
                 mbar_arrive(&q_empty[qs]);
             }
+            LZ_TRACE(pc, 2);
         }
         // State hand-off: the last min(L, w) keys and values into the ring
         // (token p0 + tau in slot (p0 + tau) % w), pos = L (a continued
@@ -829,87 +987,219 @@ __global__ void __launch_bounds__(THREADS, 1)
                 give_up();
                 break;
             }
+            LZ_TRACE(pc, 12);
             tc_fence_after();
-            // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
-            float x[2 * NB][16];
-            float meta[META_ROWS];
-            float mx = -INFINITY;
-            {
-                uint32_t r[2 * NB][16], rm[16];
+            // Overlay of the two band chunks (w <= 64): slot s <= t holds
+            // current-chunk column s and slot s > t previous-chunk column s.
+            // Row t's window keys all sit in distinct slots (exactly the 64
+            // slots when w = 64 and the history is complete), so each thread
+            // scores 32 slots, not 64.
+            bool brk = false, fast = false;
+            if constexpr (NP == 1) fast = w <= 64;
+            if (fast) {
+                float x[2][16];
+                float mx = -INFINITY;
+                uint32_t rm[16];
+                {
+                    uint32_t rp[2][16], rc[2][16];
+                    tmem_ld16_x2<16>(tl + T_SC, rp[0]);
+                    tmem_ld16_x2<16>(tl + T_SC + 32, rp[1]);
+                    tmem_ld16_x2<16>(tl + T_SC + 64, rc[0]);
+                    tmem_ld16_x2<16>(tl + T_SC + 96, rc[1]);
+                    tmem_ld16(tl + T_SC + 128, rm);
+                    tmem_wait_ld();
+                    if (w == 64 && 64 - c0 - nvalid <= 1) {
+                        // every slot is a key of its row
 #pragma unroll
-                for (int jj = 0; jj < 2 * NB; ++jj) tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r[jj]);
-                tmem_ld16(tl + T_SC + 64 * NB, rm);
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int dj = t - 16 * hs - 32 * jj;  // slot 32 jj + 16 hs + e <= t iff e <= dj
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                x[jj][e] = __uint_as_float(e <= dj ? rc[jj][e] : rp[jj][e]);
+                                mx = fmaxf(mx, x[jj][e]);
+                            }
+                        }
+                    } else {
+                        // slot s is a key iff its band column (64 + s current,
+                        // s previous) is at least lo
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int dj = t - 16 * hs - 32 * jj;
+                            const int lc = lo - 64 - 16 * hs - 32 * jj, lp = lo - 16 * hs - 32 * jj;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const bool cur = e <= dj;
+                                const bool key = e >= (cur ? lc : lp);
+                                x[jj][e] = key ? __uint_as_float(cur ? rc[jj][e] : rp[jj][e]) : -INFINITY;
+                                mx = fmaxf(mx, x[jj][e]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < META_ROWS; ++e) {
+                    if (e >= m) break;
+                    if (hs == 0) mx = fmaxf(mx, __uint_as_float(rm[e]));
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                LZ_TRACE(pc, 22);
+                const float2 M2 = make_float2(-mx * LOG2E, -mx * LOG2E), L2E = make_float2(LOG2E, LOG2E);
+                float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 z = fma2(make_float2(x[jj][e], x[jj][e + 1]), L2E, M2);
+                        x[jj][e] = ex2(z.x);
+                        x[jj][e + 1] = ex2(z.y);
+                        sum2 = add2(sum2, make_float2(x[jj][e], x[jj][e + 1]));
+                    }
+                float sum = sum2.x + sum2.y;
+#pragma unroll
+                for (int e = 0; e < META_ROWS; ++e) {
+                    if (e >= m) break;
+                    if (hs == 0) sum += ex2(fmaf(__uint_as_float(rm[e]), LOG2E, M2.x));
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+                LZ_TRACE(pc, 23);
+                const float inv = alpha / sum;
+                if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
+                               [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
+                    give_up();
+                    break;
+                }
+                uint32_t ra2[2][16];  // intra-chunk scores A of this thread's slots
+                tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
+                tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
                 tmem_wait_ld();
+                // SC and A are read: the next chunk's scores may overwrite them
+                tc_fence_before();
+                named_bar(NB_SOFT, SOFT_N);
+                if (st_ == 0) mbar_arrive(sc_free);
+                LZ_TRACE(pc, 13);
+                const float2 inv2 = make_float2(rowok ? inv : 0.f, rowok ? inv : 0.f);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int dj = t - 16 * hs - 32 * jj;
+                    uint32_t pp[8], pq[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 v = mul2(make_float2(x[jj][e], x[jj][e + 1]), inv2);
+                        const float2 av = make_float2(rowok ? __uint_as_float(ra2[jj][e]) : 0.f,
+                                                      rowok ? __uint_as_float(ra2[jj][e + 1]) : 0.f);
+                        const float2 vc = add2(v, av);
+                        const bool c0_ = e <= dj, c1_ = e + 1 <= dj;
+                        pp[e / 2] = f2_to_bf2(c0_ ? 0.f : v.x, c1_ ? 0.f : v.y);
+                        pq[e / 2] = f2_to_bf2(c0_ ? vc.x : 0.f, c1_ ? vc.y : 0.f);
+                    }
+                    const int col = 32 * jj + 16 * hs;
+                    *reinterpret_cast<uint4 *>(sm + SM::W + sw128_offset(t, col * 2)) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+                    *reinterpret_cast<uint4 *>(sm + SM::W + sw128_offset(t, col * 2 + 16)) = make_uint4(pp[4], pp[5], pp[6], pp[7]);
+                    *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+                    *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2 + 16)) = make_uint4(pq[4], pq[5], pq[6], pq[7]);
+                }
+            } else {
+                // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
+                float x[2 * NB][16];
+                float meta[META_ROWS];
+                float mx = -INFINITY;
+                {
+                    uint32_t r[2 * NB][16], rm[16];
+#pragma unroll
+                    for (int jj = 0; jj < 2 * NB; ++jj) tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r[jj]);
+                    tmem_ld16(tl + T_SC + 64 * NB, rm);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 2 * NB; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            // band column 32 jj + 16 hs + e is a key of this row iff lo <= col <= hi
+                            const bool valid = (uint32_t)(d0 + 32 * jj + e) <= span;
+                            x[jj][e] = valid ? __uint_as_float(r[jj][e]) : -INFINITY;
+                            mx = fmaxf(mx, x[jj][e]);
+                        }
+#pragma unroll
+                    for (int e = 0; e < META_ROWS; ++e) {
+                        meta[e] = (hs == 0 && e < m) ? __uint_as_float(rm[e]) : -INFINITY;
+                        mx = fmaxf(mx, meta[e]);
+                    }
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                LZ_TRACE(pc, 22);
+                const float M2 = mx * LOG2E;
+                float sum = 0.f;
 #pragma unroll
                 for (int jj = 0; jj < 2 * NB; ++jj)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        // band column 32 jj + 16 hs + e is a key of this row iff lo <= col <= hi
-                        const bool valid = (uint32_t)(d0 + 32 * jj + e) <= span;
-                        x[jj][e] = valid ? __uint_as_float(r[jj][e]) : -INFINITY;
-                        mx = fmaxf(mx, x[jj][e]);
+                        x[jj][e] = ex2(fmaf(x[jj][e], LOG2E, -M2));
+                        sum += x[jj][e];
                     }
 #pragma unroll
-                for (int e = 0; e < META_ROWS; ++e) {
-                    meta[e] = (hs == 0 && e < m) ? __uint_as_float(rm[e]) : -INFINITY;
-                    mx = fmaxf(mx, meta[e]);
+                for (int e = 0; e < META_ROWS; ++e)
+                    if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
+                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+                LZ_TRACE(pc, 23);
+                const float inv = alpha / sum;
+                if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
+                               [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
+                    give_up();
+                    brk = true;
                 }
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float M2 = mx * LOG2E;
-            float sum = 0.f;
+                if (!brk) {
+                    // W in bf16: 16 band columns col0 .. col0 + 15 of row t
+                    auto store_w = [&](int col0, const uint32_t (&pk)[8]) {
+                        const uint32_t blk = (col0 / 64) * KB_T, byte = (col0 % 64) * 2;
+                        *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
+                            make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    };
+                    // the previous chunks' band columns
 #pragma unroll
-            for (int jj = 0; jj < 2 * NB; ++jj)
+                    for (int jj = 0; jj < 2 * NP; ++jj) {
+                        uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    x[jj][e] = ex2(fmaf(x[jj][e], LOG2E, -M2));
-                    sum += x[jj][e];
-                }
-#pragma unroll
-            for (int e = 0; e < META_ROWS; ++e)
-                if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
-            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            const float inv = alpha / sum;
-            if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
-                           [&] { return pc == 0 || bwait(w_free, pc - 1, abort_f); })) {
-                give_up();
-                break;
-            }
-            uint32_t ra2[2][16];  // intra-chunk scores of this thread's current-chunk columns
-            tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
-            tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 2 * NB; ++jj) {
-                const int col0 = 32 * jj + 16 * hs;  // this thread's band columns col0 .. col0 + 15
-                const bool cur = jj >= 2 * NP;       // current chunk: add the intra-chunk scores
-                const uint32_t *ra = ra2[cur ? jj - 2 * NP : 0];
-                uint32_t packed[8];
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float wv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = col0 + e + u, sidx = col - 64 * NP;
-                        float v = x[jj][e + u] * inv;
-                        if (cur && sidx <= t) v += __uint_as_float(ra[e + u]);
-                        wv[u] = rowok ? v : 0.f;
+                        for (int e = 0; e < 16; e += 2)
+                            pk[e / 2] = rowok ? f2_to_bf2(x[jj][e] * inv, x[jj][e + 1] * inv) : 0u;
+                        store_w(32 * jj + 16 * hs, pk);
                     }
-                    packed[e / 2] = f2_to_bf2(wv[0], wv[1]);
+                    // the current chunk's: plus the intra-chunk scores A (s <= t)
+                    {
+                        uint32_t ra2[2][16];
+                        tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
+                        tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
+                        tmem_wait_ld();
+                        // SC and A are read: the next chunk's scores may overwrite them
+                        tc_fence_before();
+                        named_bar(NB_SOFT, SOFT_N);
+                        if (st_ == 0) mbar_arrive(sc_free);
+                        LZ_TRACE(pc, 13);
+#pragma unroll
+                        for (int jc = 0; jc < 2; ++jc) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                float wv[2];
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    const int sidx = 32 * jc + 16 * hs + e + u;  // column within the current chunk
+                                    float v = x[2 * NP + jc][e + u] * inv;
+                                    if (sidx <= t) v += __uint_as_float(ra2[jc][e + u]);
+                                    wv[u] = rowok ? v : 0.f;
+                                }
+                                pk[e / 2] = f2_to_bf2(wv[0], wv[1]);
+                            }
+                            store_w(64 * NP + 32 * jc + 16 * hs, pk);
+                        }
+                    }
                 }
-                const uint32_t blk = (col0 / 64) * KB_T, byte = (col0 % 64) * 2;
-                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte)) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
-                    make_uint4(packed[4], packed[5], packed[6], packed[7]);
             }
-            tc_fence_before();
+            if (brk) break;
             fence_proxy_async_smem();
             named_bar(NB_SOFT, SOFT_N);
-            if (st_ == 0) {
-                mbar_arrive(sc_free);
-                mbar_arrive(w_full);
-            }
+            if (st_ == 0) mbar_arrive(w_full);
+            LZ_TRACE(pc, 14);
         }
     }
 
