@@ -241,13 +241,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-// Per-warpgroup register budgets (setmaxnreg): the CTA launches with
-// 640 threads x 96 registers = 61440; the TMA / MMA warpgroup drops to 40 and
-// the gate-prep and softmax warpgroups rise to 112:
-// 40*128 + 96*128 + 112*256 + 112*128 = 60416 <= 61440.
-template <uint32_t N> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-template <uint32_t N> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
-constexpr uint32_t REG_IO = 40, REG_WIDE = 112;
 __device__ __forceinline__ uint32_t tlane(uint32_t quarter) { return (32u * quarter) << 16; }
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ bool named_bar_and(int id, int n, bool p)
@@ -321,6 +314,21 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t use, volatile int 
         if (*abort_flag) return false;
     }
     return false;
+}
+
+// One product D (+)= A B^T of bf16 tiles in shared memory, K = 16 * nk.
+// Both operand descriptors advance by (step_a, step_b) bytes per k-step and
+// by (blk_a, blk_b) bytes after every fourth step (next 64-wide block of a
+// 128-byte-swizzled K-major tile).  A rolled loop keeps the issuing code
+// small: the instruction cache is shared by every role of the CTA.
+__device__ __forceinline__ void mma_chain(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc, int nk,
+                                          uint32_t step_a, uint32_t step_b, uint32_t blk_a, uint32_t blk_b)
+{
+#pragma unroll 1
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint32_t oa = ((kk >> 2) * blk_a + (kk & 3) * step_a) >> 4, ob = ((kk >> 2) * blk_b + (kk & 3) * step_b) >> 4;
+        mma_bf16_ss(d, da + oa, db + ob, idesc, acc | (uint32_t)(kk > 0));
+    }
 }
 
 template <int NP>
@@ -524,16 +532,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
                 // window + meta logits
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j <= NP; ++j) {
                     const int cj = c - NP + j;
                     if (cj < c_lo) continue;
                     const uint32_t kb = sb + SM::KV + ((cj - c_lo) % NR) * SLOT;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ss(tmem + T_SC + 64 * j, smem_desc(qb + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
-                                    smem_desc(kb + (kk / 4) * KB_K + (kk % 4) * 32, 16, 1024),
-                                    j == NP ? id_sc_cur : id_sc_prev, kk > 0);
+                    mma_chain(tmem + T_SC + 64 * j, smem_desc(qb, 16, 1024), smem_desc(kb, 16, 1024),
+                              j == NP ? id_sc_cur : id_sc_prev, 0u, 8, 32, 32, KB_T, KB_K);
                 }
                 mma_commit(sc_full);
                 mma_commit(&q_empty[qs]);
@@ -543,11 +548,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 if (!unsafe_f[b]) {
                     const uint32_t ob = sb + SM::OP + b * OPB;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ss(tmem + TM::A, smem_desc(ob + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024),
-                                    smem_desc(ob + 2 * KB_T + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_a,
-                                    kk > 0);
+                    mma_chain(tmem + TM::A, smem_desc(ob, 16, 1024), smem_desc(ob + 2 * KB_T, 16, 1024), id_a, 0u, 8,
+                              32, 32, KB_T, KB_T);
                     mma_commit(a_full);
                 } else {
                     mbar_arrive(a_full);  // exact A, stored by the prep role before op_full
@@ -577,10 +579,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 // Shat^T += V^T K, K = KR (KL for an unsafe chunk)
                 const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V, kb = sb + SM::OP + b * OPB + 2 * KB_T;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + T_S, smem_desc(vb + kk * 2048, KB_T, 1024),
-                                smem_desc(kb + kk * 2048, KB_T, 1024), id_st, 1u);
+                mma_chain(tmem + T_S, smem_desc(vb, KB_T, 1024), smem_desc(kb, KB_T, 1024), id_st, 1u, 4, 2048, 2048, 0,
+                          0);
                 mma_commit(st_done);
                 mma_commit(&op_free[b]);
                 mma_commit(&v_empty[s]);
@@ -602,10 +602,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     (pc >= 1 && !bwait(y_free, pc - 1, abort_f))) { give_up(); break; }
                 tc_fence_after();
                 const uint32_t ob = sb + SM::OP + b * OPB;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8,
-                                smem_desc(ob + (kk / 4) * KB_T + (kk % 4) * 32, 16, 1024), id_y1, kk > 0);
+                {
+                    const uint64_t dq = smem_desc(ob, 16, 1024);
+#pragma unroll 1
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8, dq + ((((kk >> 2) * KB_T) + (kk & 3) * 32) >> 4),
+                                    id_y1, kk > 0);
+                }
                 mma_commit(s16_free);
                 mma_commit(&op_free[b]);
                 LZ_TRACE(pc, 6);
@@ -613,15 +616,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!bwait(w_full, pc, abort_f) || !bwait(&v_full[r % NR], r / NR, abort_f) ||
                     (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f))) { give_up(); break; }
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j <= NP; ++j) {
                     const int cj = c - NP + j;
                     if (cj < c_lo) continue;
                     const uint32_t vb = sb + SM::KV + ((cj - c_lo) % NR) * SLOT + SLOT_V;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + T_Y, smem_desc(vb + kk * 2048, KB_T, 1024),
-                                    smem_desc(sb + SM::W + j * KB_T + kk * 32, 16, 1024), id_y2, 1u);
+                    mma_chain(tmem + T_Y, smem_desc(vb, KB_T, 1024), smem_desc(sb + SM::W + j * KB_T, 16, 1024), id_y2,
+                              1u, 4, 2048, 32, 0, 0);
                 }
                 mma_commit(y_full);
                 mma_commit(w_free);
@@ -860,35 +861,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // Scratch: the other operand buffer holds b (fp32, [64][128])
                 // meanwhile; its chunk's products and the previous softmax
                 // (which read the A columns) are done.
-                float2 cs[16];
-                {
-                    float2 run = make_float2(0.f, 0.f);
-                    const int t0 = c * C + 16 * hq;
-#pragma unroll
-                    for (int tt = 0; tt < 16; ++tt) {
-                        const uint32_t gv =
-                            t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
-                        run = add2(run, log2_sigmoid2(bf2_to_f2(gv)));
-                        cs[tt] = run;
-                    }
-                    *reinterpret_cast<float2 *>(tot + hq * 128 + 2 * p) = run;
-                }
                 if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N, [&] {
                         return pc == 0 ||
                                (bwait(&op_free[b ^ 1], (pc - 1) >> 1, abort_f) && bwait(sc_free, pc - 1, abort_f));
                     })) { give_up(); break; }
-                float2 Tl[4];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) Tl[qq] = *reinterpret_cast<const float2 *>(tot + qq * 128 + 2 * p);
-                float2 pre = make_float2(0.f, 0.f);  // b at the end of the previous quarter
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    if (qq < hq) pre = add2(pre, Tl[qq]);
-                const float2 blast = add2(add2(Tl[0], Tl[1]), add2(Tl[2], Tl[3]));
                 float *bz = reinterpret_cast<float *>(sm + SM::OP + (b ^ 1) * OPB);
+                {
+                    // the quarter's prefix sums into the scratch, its total to tot
+                    float2 run = make_float2(0.f, 0.f);
+                    const int t0 = c * C + 16 * hq;
+#pragma unroll 1
+                    for (int tt = 0; tt < 16; ++tt) {
+                        const uint32_t gv =
+                            t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
+                        run = add2(run, log2_sigmoid2(bf2_to_f2(gv)));
+                        *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) = run;
+                    }
+                    *reinterpret_cast<float2 *>(tot + hq * 128 + 2 * p) = run;
+                }
+                named_bar(NB_PREP, PREP_N);
+                float2 pre = make_float2(0.f, 0.f), blast = make_float2(0.f, 0.f);  // b before the quarter, b_last
 #pragma unroll
-                for (int tt = 0; tt < 16; ++tt)
-                    *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) = add2(cs[tt], pre);
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float2 Tq = *reinterpret_cast<const float2 *>(tot + qq * 128 + 2 * p);
+                    if (qq < hq) pre = add2(pre, Tq);
+                    blast = add2(blast, Tq);
+                }
+#pragma unroll 1
+                for (int tt = 0; tt < 16; ++tt) {
+                    float2 *bp = reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p);
+                    *bp = add2(*bp, pre);
+                }
                 named_bar(NB_PREP, PREP_N);
                 {
                     const int quarter = warp & 3, li = ((warp - W_PREP) >> 2) * 32 + lane;
@@ -921,7 +924,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 named_bar(NB_PREP, PREP_N);
                 // QR with r = 0 (exponents <= 0); the key operand is KL, F = 1.
-#pragma unroll
+#pragma unroll 1
                 for (int tt = 0; tt < 16; ++tt) {
                     const int t = 16 * hq + tt;
                     const uint32_t off = sw128_offset(t, kbyte);
@@ -980,8 +983,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Keys of row t: positions max(-nvalid, tg - w + 1) .. tg, i.e.
             // band columns lo .. hi.
             const int hi = t + 64 * NP, lo = max(-pbase - nvalid, hi - w + 1);
-            const int d0 = 16 * hs - lo;
-            const uint32_t span = (uint32_t)(hi - lo);
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
                            [&] { return bwait(sc_full, pc, abort_f) && bwait(a_full, pc, abort_f); })) {
                 give_up();
@@ -1099,45 +1100,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2 + 16)) = make_uint4(pq[4], pq[5], pq[6], pq[7]);
                 }
             } else {
-                // band columns of this thread: group 2j + hs (16 columns each), j < 2 NB
-                float x[2 * NB][16];
-                float meta[META_ROWS];
+                // Every band column scored separately (w = 65, or a window of
+                // one token), in three passes over tensor memory -- max, sum,
+                // weights -- so that one 16-column group is held at a time.
+                const int d0 = 16 * hs - lo;
+                const uint32_t span = (uint32_t)(hi - lo);
+                uint32_t rm[16];
+                tmem_ld16(tl + T_SC + 64 * NB, rm);
                 float mx = -INFINITY;
-                {
-                    uint32_t r[2 * NB][16], rm[16];
-#pragma unroll
-                    for (int jj = 0; jj < 2 * NB; ++jj) tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r[jj]);
-                    tmem_ld16(tl + T_SC + 64 * NB, rm);
+#pragma unroll 1
+                for (int jj = 0; jj < 2 * NB; ++jj) {
+                    uint32_t r[16];
+                    tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 2 * NB; ++jj)
+                    for (int e = 0; e < 16; ++e)
+                        if ((uint32_t)(d0 + 32 * jj + e) <= span) mx = fmaxf(mx, __uint_as_float(r[e]));
+                }
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            // band column 32 jj + 16 hs + e is a key of this row iff lo <= col <= hi
-                            const bool valid = (uint32_t)(d0 + 32 * jj + e) <= span;
-                            x[jj][e] = valid ? __uint_as_float(r[jj][e]) : -INFINITY;
-                            mx = fmaxf(mx, x[jj][e]);
-                        }
-#pragma unroll
-                    for (int e = 0; e < META_ROWS; ++e) {
-                        meta[e] = (hs == 0 && e < m) ? __uint_as_float(rm[e]) : -INFINITY;
-                        mx = fmaxf(mx, meta[e]);
-                    }
+                for (int e = 0; e < META_ROWS; ++e) {
+                    if (e >= m) break;
+                    if (hs == 0) mx = fmaxf(mx, __uint_as_float(rm[e]));
                 }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 LZ_TRACE(pc, 22);
                 const float M2 = mx * LOG2E;
                 float sum = 0.f;
+#pragma unroll 1
+                for (int jj = 0; jj < 2 * NB; ++jj) {
+                    uint32_t r[16];
+                    tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 2 * NB; ++jj)
+                    for (int e = 0; e < 16; ++e)
+                        if ((uint32_t)(d0 + 32 * jj + e) <= span) sum += ex2(fmaf(__uint_as_float(r[e]), LOG2E, -M2));
+                }
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        x[jj][e] = ex2(fmaf(x[jj][e], LOG2E, -M2));
-                        sum += x[jj][e];
-                    }
-#pragma unroll
-                for (int e = 0; e < META_ROWS; ++e)
-                    if (hs == 0 && e < m) sum += ex2(fmaf(meta[e], LOG2E, -M2));
+                for (int e = 0; e < META_ROWS; ++e) {
+                    if (e >= m) break;
+                    if (hs == 0) sum += ex2(fmaf(__uint_as_float(rm[e]), LOG2E, -M2));
+                }
                 sum += __shfl_xor_sync(0xffffffffu, sum, 16);
                 LZ_TRACE(pc, 23);
                 const float inv = alpha / sum;
@@ -1147,52 +1149,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                     brk = true;
                 }
                 if (!brk) {
-                    // W in bf16: 16 band columns col0 .. col0 + 15 of row t
-                    auto store_w = [&](int col0, const uint32_t (&pk)[8]) {
+                    // W = alpha P / Z, plus A (s <= t) in the current chunk's columns
+#pragma unroll 1
+                    for (int jj = 0; jj < 2 * NB; ++jj) {
+                        const bool cur = jj >= 2 * NP;
+                        uint32_t r[16], ra[16];
+                        tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
+                        tmem_ld16_x2<16>(tl + TM::A + 32 * (cur ? jj - 2 * NP : 0), ra);
+                        tmem_wait_ld();
+                        const int col0 = 32 * jj + 16 * hs;
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            float wv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const bool key = (uint32_t)(d0 + 32 * jj + e + u) <= span;
+                                float v = key ? ex2(fmaf(__uint_as_float(r[e + u]), LOG2E, -M2)) * inv : 0.f;
+                                if (cur && col0 + e + u - 64 * NP <= t) v += __uint_as_float(ra[e + u]);
+                                wv[u] = rowok ? v : 0.f;
+                            }
+                            pk[e / 2] = f2_to_bf2(wv[0], wv[1]);
+                        }
                         const uint32_t blk = (col0 / 64) * KB_T, byte = (col0 % 64) * 2;
                         *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte)) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
                             make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    };
-                    // the previous chunks' band columns
-#pragma unroll
-                    for (int jj = 0; jj < 2 * NP; ++jj) {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int e = 0; e < 16; e += 2)
-                            pk[e / 2] = rowok ? f2_to_bf2(x[jj][e] * inv, x[jj][e + 1] * inv) : 0u;
-                        store_w(32 * jj + 16 * hs, pk);
                     }
-                    // the current chunk's: plus the intra-chunk scores A (s <= t)
-                    {
-                        uint32_t ra2[2][16];
-                        tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
-                        tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
-                        tmem_wait_ld();
-                        // SC and A are read: the next chunk's scores may overwrite them
-                        tc_fence_before();
-                        named_bar(NB_SOFT, SOFT_N);
-                        if (st_ == 0) mbar_arrive(sc_free);
-                        LZ_TRACE(pc, 13);
-#pragma unroll
-                        for (int jc = 0; jc < 2; ++jc) {
-                            uint32_t pk[8];
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                float wv[2];
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const int sidx = 32 * jc + 16 * hs + e + u;  // column within the current chunk
-                                    float v = x[2 * NP + jc][e + u] * inv;
-                                    if (sidx <= t) v += __uint_as_float(ra2[jc][e + u]);
-                                    wv[u] = rowok ? v : 0.f;
-                                }
-                                pk[e / 2] = f2_to_bf2(wv[0], wv[1]);
-                            }
-                            store_w(64 * NP + 32 * jc + 16 * hs, pk);
-                        }
-                    }
+                    // SC and A are read: the next chunk's scores may overwrite them
+                    tc_fence_before();
+                    named_bar(NB_SOFT, SOFT_N);
+                    if (st_ == 0) mbar_arrive(sc_free);
+                    LZ_TRACE(pc, 13);
                 }
             }
             if (brk) break;
