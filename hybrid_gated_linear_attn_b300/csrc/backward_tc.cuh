@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                         const __grid_constant__ CUtensorMap tdy, const StatesArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     float *dec = reinterpret_cast<float *>(sm + ST_VEC), *tot = dec + 128;
     uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + ST_BAR), *bar_mma = bar_tma + 2;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                      const QueryArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     float *rv = reinterpret_cast<float *>(sm + QO_VEC), *tot = rv + 128, *dC = tot + 512;
     int *flags = reinterpret_cast<int *>(dC + 64 * 16);
@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const KeyArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     float *rv = reinterpret_cast<float *>(sm + KO_VEC), *blv = rv + 128, *tot = blv + 128, *Ep = tot + 512;
     float *bk = reinterpret_cast<float *>(sm + KO_B);  // phase B: b [64][128]

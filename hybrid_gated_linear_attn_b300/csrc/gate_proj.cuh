@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int BN = G::BN;
     constexpr uint32_t A_BYTES = G::A_BYTES, STAGE = G::STAGE, OFF_BAR = G::OFF_BAR;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + OFF_BAR), *empty = full + STAGES, *done = empty + STAGES;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                          const __grid_constant__ CUtensorMap tg, const SegArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     float *tot = reinterpret_cast<float *>(sm + OFF_TOT);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);

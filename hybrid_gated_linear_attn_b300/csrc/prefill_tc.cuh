@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int NB = NP + 1;     // band chunks
     constexpr int PART = 16 * NB;  // band columns per softmax thread (four threads per row)
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     float *xch = reinterpret_cast<float *>(sm + OFF_VEC);  // [token quarter 4][128]
     float *first2 = xch + 512, *last2 = first2 + 128, *dec = last2 + 128;

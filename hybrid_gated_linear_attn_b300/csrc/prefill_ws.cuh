@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int NR = SM::NR;
     constexpr int NB = NP + 1;  // band chunks
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     // Scale vectors of operand buffer b: vec + b * NVEC * 128 -> sig (state
     // pass: Shat scale), tau (S16 scale), F (the chunk's state factor).

@@ -21,6 +21,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory window rounded up to a 1024-byte boundary (the
+// 128-byte swizzle atom).  The offset is added to the shared pointer itself
+// so that the compiler keeps it in the shared state space (native 32-bit
+// shared loads and stores, not generic ones).
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *raw)
+{
+    const uint32_t a = smem_u32(raw);
+    return raw + (((a + 1023u) & ~1023u) - a);
+}
+
 // Byte offset of byte `byte_in_row` of row `row` in a 128B-swizzled tile
 // whose rows are 128 B (tile base 1024-byte aligned).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row)
