@@ -664,18 +664,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const int c0 = (c_begin + py) * C, n = min(C, L - c0);
             __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
-#pragma unroll 1
-            for (int cc = 0; cc < C; cc += 16) {
-                uint32_t r[16];
-                tmem_ld16(tl + T_Y + cc, r);
-                tmem_wait_ld();
+            uint32_t r[4][16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (cc + e < n) yp[(size_t)(cc + e) * D] = __float2bfloat16_rn(__uint_as_float(r[e]));
-            }
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tl + T_Y + 16 * q4, r[q4]);
+            tmem_wait_ld();
+            // the accumulator is read: the next chunk's products may start
             tc_fence_before();
             named_bar(NB_EPI, EPI_N);
             if (et == 0) mbar_arrive(y_free);
+            // Lanes j, j^1 trade halves of a token pair, so that each stores
+            // two adjacent value dims of one token (4-byte stores): the even
+            // lane token t, the odd lane token t + 1.
+            const bool odd = lane & 1;
+            __nv_bfloat16 *yq = yp - (odd ? 1 : 0) + (odd ? D : 0);
+            const int t_odd = odd ? 1 : 0;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const uint32_t mine = f2_to_bf2(__uint_as_float(r[q4][e]), __uint_as_float(r[q4][e + 1]));
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                    // even: (mine.lo, other.lo); odd: (other.hi, mine.hi)
+                    const uint32_t out = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
+                    if (16 * q4 + e + t_odd < n)
+                        *reinterpret_cast<uint32_t *>(yq + (size_t)(16 * q4 + e) * D) = out;
+                }
             LZ_TRACE(py, 11);
             return true;
         };
@@ -998,9 +1011,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool brk = false, fast = false;
             if constexpr (NP == 1) fast = w <= 64;
             if (fast) {
+                // Read SC and A first and release their columns at once, so
+                // that the next chunk's score products overlap this softmax.
                 float x[2][16];
                 float mx = -INFINITY;
-                uint32_t rm[16];
+                uint32_t rm[16], ra2[2][16];
                 {
                     uint32_t rp[2][16], rc[2][16];
                     tmem_ld16_x2<16>(tl + T_SC, rp[0]);
@@ -1037,6 +1052,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
+                tmem_ld16_x2<16>(tl + TM::A, ra2[0]);  // intra-chunk scores A of this thread's slots
+                tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                named_bar(NB_SOFT, SOFT_N);
+                if (st_ == 0) mbar_arrive(sc_free);
+                LZ_TRACE(pc, 13);
 #pragma unroll
                 for (int e = 0; e < META_ROWS; ++e) {
                     if (e >= m) break;
@@ -1069,15 +1091,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     give_up();
                     break;
                 }
-                uint32_t ra2[2][16];  // intra-chunk scores A of this thread's slots
-                tmem_ld16_x2<16>(tl + TM::A, ra2[0]);
-                tmem_ld16_x2<16>(tl + TM::A + 32, ra2[1]);
-                tmem_wait_ld();
-                // SC and A are read: the next chunk's scores may overwrite them
-                tc_fence_before();
-                named_bar(NB_SOFT, SOFT_N);
-                if (st_ == 0) mbar_arrive(sc_free);
-                LZ_TRACE(pc, 13);
                 const float2 inv2 = make_float2(rowok ? inv : 0.f, rowok ? inv : 0.f);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
