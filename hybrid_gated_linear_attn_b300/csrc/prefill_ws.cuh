@@ -37,9 +37,9 @@
 //
 // Warp roles (20 warps):
 //   warp 0       TMA producer: q, k, v tiles (k/v ring of NP+2); L2 prefetch of g
-//   warp 1       MMA issuer (one thread): scores SC and A
+//   warp 1       MMA issuer (one thread): window and meta scores SC
 //   warp 2       MMA issuer (one thread): the two output products
-//   warp 3       MMA issuer (one thread): the state update
+//   warp 3       MMA issuer (one thread): intra-chunk scores A, the state update
 //   warps 4-7    state pass (Shat scale, S16) and the y epilogue (one chunk
 //                behind); the final state
 //   warps 8-15   gate prep: log-sigmoid (g read into registers one chunk
@@ -387,13 +387,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < NR; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], 2);   // band scores + prep read the raw keys
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 2);   // state update + output products
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&op_full[i], 1);
-            mbar_init(&op_free[i], 3);   // A, the readout, the state update
+            mbar_init(&op_free[i], 2);   // A + state update, the readout
         }
         for (int i = 0; i < 13; ++i) mbar_init(&sc_full[i], 1);
         unsafe_f[0] = 0;
@@ -518,14 +518,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else if (warp == W_MMA) {
-        // ------------------------------------------------------ MMA issuer: scores SC and A
+        // ------------------------------------------------------ MMA issuer: scores SC
         if (lane == 0) {
             const uint32_t id_sc_prev = instr_desc(64, 64, FMT_BF16, 0, 0);
             const uint32_t id_sc_cur = instr_desc(64, 64 + META_ROWS, FMT_BF16, 0, 0);
-            const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
             for (int c = c_begin; c < c_end; ++c) {
                 const int pc = c - c_begin, r = c - c_lo;
-                const int s = r % NR, qs = pc % QS, b = pc & 1;
+                const int s = r % NR, qs = pc % QS;
                 const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
                 if ((pc == 0 && c_lo < c_begin && !bwait(&k_full[0], 0, abort_f)) ||
                     !bwait(&k_full[s], r / NR, abort_f) || !bwait(&q_full[qs], pc / QS, abort_f) ||
@@ -543,8 +542,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_commit(sc_full);
                 mma_commit(&q_empty[qs]);
                 LZ_TRACE(pc, 3);
-                // intra-chunk decayed scores
-                if (!bwait(&op_full[b], pc >> 1, abort_f)) { give_up(); break; }
+                // The key tile of chunk c - NP: its last band scores are issued.
+                if (c - NP >= c_lo) mma_commit(&k_empty[(c - NP - c_lo) % NR]);
+            }
+            // Drain: every product issued has completed before tensor memory is released.
+            mma_commit(drain);
+            bwait(drain, 0, abort_f);
+        }
+        __syncwarp();
+    } else if (warp == W_MMAS) {
+        // ------------------------------------------------------ MMA issuer: intra-chunk scores A, state update
+        if (lane == 0) {
+            const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
+            const uint32_t id_a = instr_desc(64, 64, FMT_BF16, 0, 0);
+            // band chunks before the segment get no state update and no prep
+            for (int c = c_lo; c < c_begin; ++c) {
+                mbar_arrive(&v_empty[(c - c_lo) % NR]);
+                mbar_arrive(&k_empty[(c - c_lo) % NR]);
+            }
+            for (int c = c_begin; c < c_end; ++c) {
+                const int pc = c - c_begin, r = c - c_lo, s = r % NR, b = pc & 1;
+                // intra-chunk decayed scores A (the A columns are free once the
+                // previous chunk's softmax has read them)
+                if (!bwait(&op_full[b], pc >> 1, abort_f) || (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) {
+                    give_up();
+                    break;
+                }
+                LZ_TRACE(pc, 28);
                 tc_fence_after();
                 if (!unsafe_f[b]) {
                     const uint32_t ob = sb + SM::OP + b * OPB;
@@ -555,27 +579,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive(a_full);  // exact A, stored by the prep role before op_full
                 }
                 LZ_TRACE(pc, 4);
-                // The key tile of chunk c - NP has no reader left: the last
-                // band scores that use it were issued above, and its raw keys
-                // were read by the prep of chunk c - NP (done: op_full).
-                if (c - NP >= c_lo) mma_commit(&k_empty[(c - NP - c_lo) % NR]);
-                mma_commit(&op_free[b]);
-            }
-            // Drain: every product issued has completed before tensor memory is released.
-            mma_commit(drain);
-            bwait(drain, 0, abort_f);
-        }
-        __syncwarp();
-    } else if (warp == W_MMAS) {
-        // ------------------------------------------------------ MMA issuer: state update
-        if (lane == 0) {
-            const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
-            // band chunks before the segment get no state update here
-            for (int c = c_lo; c < c_begin; ++c) mbar_arrive(&v_empty[(c - c_lo) % NR]);
-            for (int c = c_begin; c < c_end; ++c) {
-                const int pc = c - c_begin, r = c - c_lo, s = r % NR, b = pc & 1;
-                if (!bwait(s_ready, pc, abort_f) || !bwait(&op_full[b], pc >> 1, abort_f) ||
-                    !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
+                mbar_arrive(&k_empty[s]);  // the prep of this chunk has read its raw keys
+                if (!bwait(s_ready, pc, abort_f) || !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
                 tc_fence_after();
                 // Shat^T += V^T K, K = KR (KL for an unsafe chunk)
                 const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V, kb = sb + SM::OP + b * OPB + 2 * KB_T;
