@@ -193,6 +193,11 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def workload_name(wl) -> str:
+    """The bench workload, named the same way by both arms."""
+    return f"llama3_8b prefill B{wl.B} H{wl.H} L{wl.L} d{wl.dk} w{wl.w} m{wl.m} {wl.dtype}"
+
+
 def rank_seed(base: int, rank: int) -> int:
     """Each rank draws its own sequences (weak scaling over the batch)."""
     return base + 1000 * rank
@@ -239,8 +244,8 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "llama3_8b prefill B4 H32 L4096 d128 w64 m4 (fp64 CPU oracle)",
-                   "global_batch": wl.B, "seq_len": wl.L},
+        "config": {"workload": workload_name(wl), "global_batch": wl.B, "seq_len": wl.L,
+                   "implementation": "fp64 CPU oracle"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -361,6 +366,23 @@ def run_ours(args, world, rank, local):
         psteps = max(3, min(args.steps, 10))
         pms = max_over_ranks(time_loop(pstep, psteps, max(args.warmup, 2), stream), world)
         pflops = 2.0 * Bl * wl.L * wl.H * wl.dk * dmodel
+
+        # ---- the decay-stress and long-context prefill workloads, same run ----
+        extra = {}
+        for name in ("decay_stress", "long_context"):
+            xwl = WORKLOADS[name]
+            xin = prefill_inputs(xwl, seed=rank_seed(xwl.seed, rank))
+            xq, xk, xv, xg, xmu = (xin[n].cuda() for n in ("q", "k", "v", "g", "mu"))
+            xy = torch.empty_like(xv)
+            xst = LizardState(xwl.B, xwl.H, xwl.dk, xwl.dv, xwl.w, dtype=xq.dtype)
+
+            def xstep():
+                lizard_attn_prefill(xq, xk, xv, xg, xmu, xwl.alpha, xwl.w, y=xy, state=xst, stream=stream)
+
+            xsteps = max(3, min(args.steps, 10))
+            xms = max_over_ranks(time_loop(xstep, xsteps, max(args.warmup, 2), stream), world)
+            extra[name] = (xwl, xms, xsteps)
+            del xq, xk, xv, xg, xmu, xy, xst, xin
     lizard_check_device_status(stream)
     clock = clocks.summary()
 
@@ -399,8 +421,9 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)-family tensors, no dataset)",
-        "config": {"workload": f"llama3_8b prefill B{wl.B} H{wl.H} L{wl.L} d{wl.dk} w{wl.w} m{wl.m} bf16 "
-                               f"(+ decode {dwl.B}x{dwl.H} d{dwl.dk} w{dwl.w} m{dwl.m})",
+        "config": {"workload": workload_name(wl),
+                   "also_timed": f"decode {dwl.B}x{dwl.H} d{dwl.dk} w{dwl.w} m{dwl.m}; backward and gate projection "
+                                 f"of the same layer",
                    "global_batch": world * Bl, "seq_len": wl.L, "parallelism": f"dp{world} (independent sequences)",
                    "l2": "inputs larger than L2 (680 MB read/written per prefill step, 339 MB per decode step)"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -430,6 +453,17 @@ def run_ours(args, world, rank, local):
                                          "frac": pflops / (pms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                                          "peak_source": peak_src, "traffic": None, "kernel": "gate_proj_kernel",
                                          "launch_ms": pms, "algorithmic_flops": pflops}},
+        "prefill_workloads": {
+            name: {"workload": f"{name} prefill B{xwl.B} H{xwl.H} L{xwl.L} d{xwl.dk} w{xwl.w} m{xwl.m} {xwl.dtype}",
+                   "value": world * xwl.B * xwl.L / (xms * 1e-3), "unit": "tokens/s", "ms_per_step": xms,
+                   "steps": xsteps,
+                   "roofline": {"bound": "hbm", "achieved": prefill_bytes(xwl) / (xms * 1e-3) / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": prefill_bytes(xwl) / (xms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "peak_source": peak_src, "traffic": None, "launch_ms": xms,
+                                "algorithmic_bytes": prefill_bytes(xwl)},
+                   "tensor_frac": prefill_flops(xwl) / (xms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+            for name, (xwl, xms, xsteps) in extra.items()},
         "e2e": {"value": world * tokens_rank / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * 1,
@@ -492,6 +526,19 @@ def run_profile_case(args):
     return 0
 
 
+def relaunch(n: int) -> int:
+    """``--gpus N`` without a launcher: run this same script as N local ranks
+    under torch.distributed.run (one process per GPU, rendezvous on
+    127.0.0.1) and return its exit status; rank 0 prints the JSON line."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(sys.argv[0]), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,7 +554,12 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="batch override for --profile-case")
     ap.add_argument("--seq-len", type=int, default=0, help="prompt length override for --profile-case prefill")
     args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not args.profile_case:
+        return relaunch(args.gpus)
     world, rank, local = dist_setup()
+    if not args.profile_case and world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if args.profile_case:
         if args.workload is None:
             args.workload = "decode" if args.profile_case == "decode" else "llama3_8b"
@@ -516,7 +568,10 @@ def main(argv=None):
         return run_reference(args, world, rank)
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     try:
         return run_ours(args, world, rank, local)
     finally:

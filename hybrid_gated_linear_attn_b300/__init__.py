@@ -12,6 +12,8 @@ from .lizard_attn import (  # noqa: F401
     lizard_attn_prefill_noalloc,
     lizard_check_device_status,
     lizard_gate_projection,
+    lizard_scratch_reserved,
+    lizard_scratch_trim,
     lizard_state_init,
     lizard_status_string,
 )

@@ -51,38 +51,47 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // device.  Its release threshold is unlimited: memory a call frees stays
 // reserved for the library's next calls, so a steady stream of calls maps
 // no new memory (the device's default pool would hand freed memory back at
-// every synchronisation).  The caller's own allocations are untouched.
+// every synchronisation), until lizard_scratch_trim returns it.  The
+// caller's own allocations are untouched.
+static std::mutex g_pool_mu;
+static constexpr int MAX_POOL_DEV = 64;
+static cudaMemPool_t g_pools[MAX_POOL_DEV] = {};
+
+// The library's pool on device `dev`, created on first use when `create`.
+static cudaError_t scratch_pool(int dev, bool create, cudaMemPool_t *out)
+{
+    *out = nullptr;
+    if (dev < 0 || dev >= MAX_POOL_DEV) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev] && create) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t np = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&np, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(np);
+            return e;
+        }
+        g_pools[dev] = np;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+
 static cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s)
 {
-    constexpr int MAX_DEV = 64;
-    static std::mutex mu;
-    static cudaMemPool_t pools[MAX_DEV] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
     cudaMemPool_t pool;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!pools[dev]) {
-            cudaMemPoolProps props = {};
-            props.allocType = cudaMemAllocationTypePinned;
-            props.handleTypes = cudaMemHandleTypeNone;
-            props.location.type = cudaMemLocationTypeDevice;
-            props.location.id = dev;
-            cudaMemPool_t np = nullptr;
-            e = cudaMemPoolCreate(&np, &props);
-            if (e != cudaSuccess) return e;
-            uint64_t keep = UINT64_MAX;
-            e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep);
-            if (e != cudaSuccess) {
-                cudaMemPoolDestroy(np);
-                return e;
-            }
-            pools[dev] = np;
-        }
-        pool = pools[dev];
-    }
+    e = scratch_pool(dev, true, &pool);
+    if (e != cudaSuccess) return e;
     return cudaMallocFromPoolAsync(p, bytes, pool, s);
 }
 static size_t esize(lizard_dtype dt) { return dt == LIZARD_F32 ? 4 : 2; }
@@ -499,21 +508,45 @@ static bool make_rows_map(CUtensorMap *map, const void *base, int rows, int K, i
 constexpr size_t NOALLOC_FLOATS = LIZARD_NOALLOC_SCRATCH_BYTES / sizeof(float);
 static __device__ __align__(256) float g_prefill_scratch[NOALLOC_FLOATS];
 
+// The driver's cuCtxGetCurrent, looked up once (as the tensor-map encoder).
+typedef CUresult (*ctx_get_current_fn)(CUcontext *);
+static ctx_get_current_fn lookup_ctx_get_current()
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<ctx_get_current_fn>(p);
+    return nullptr;
+}
+static CUcontext current_context()
+{
+    static const ctx_get_current_fn fn = lookup_ctx_get_current();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
 // The array's device address on the current device.  In host code the name
 // g_prefill_scratch is a host-side stand-in, not a device address, so it is
-// looked up once per device (cudaGetSymbolAddress) with that device current.
+// looked up (cudaGetSymbolAddress) with the device current, once per device
+// and context: a device reset gives the device a new context in which the
+// module, and so the array, is loaded again, and the lookup is repeated.
 static lizard_status noalloc_scratch(float **out)
 {
     constexpr int MAX_DEV = 64;
     static std::mutex mu;
     static float *addr[MAX_DEV] = {};
+    static CUcontext ctx[MAX_DEV] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return LIZARD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const CUcontext now = current_context();
+    if (!addr[dev] || !now || now != ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || !p) return LIZARD_ERR_CUDA;
         addr[dev] = static_cast<float *>(p);
+        ctx[dev] = current_context();  // the lookup makes the device's context current
     }
     *out = addr[dev];
     return LIZARD_OK;
@@ -786,6 +819,31 @@ lizard_status lizard_attn_decode_step_v(const void *q, const void *k, const void
     if (st->dtype == LIZARD_BF16)
         return st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s) : launch_decode<__nv_bfloat16, 64>(da, s);
     return st->dk == 128 ? launch_decode<float, 128>(da, s) : launch_decode<float, 64>(da, s);
+}
+
+lizard_status lizard_scratch_trim(size_t keep_bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LIZARD_ERR_CUDA;
+    cudaMemPool_t pool;
+    if (scratch_pool(dev, false, &pool) != cudaSuccess) return LIZARD_ERR_CUDA;
+    if (!pool) return LIZARD_OK;
+    return cudaMemPoolTrimTo(pool, keep_bytes) == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
+}
+
+lizard_status lizard_scratch_reserved(size_t *bytes)
+{
+    if (!bytes) return LIZARD_ERR_INVALID_ARG;
+    *bytes = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LIZARD_ERR_CUDA;
+    cudaMemPool_t pool;
+    if (scratch_pool(dev, false, &pool) != cudaSuccess) return LIZARD_ERR_CUDA;
+    if (!pool) return LIZARD_OK;
+    uint64_t v = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v) != cudaSuccess) return LIZARD_ERR_CUDA;
+    *bytes = (size_t)v;
+    return LIZARD_OK;
 }
 
 lizard_status lizard_check_device_status(lizard_stream_t stream)

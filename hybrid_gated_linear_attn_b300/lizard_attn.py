@@ -26,7 +26,7 @@ LIZARD_MAX_META = 16
 EXPORTS = ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_v", "lizard_attn_prefill_continue",
            "lizard_attn_prefill_continue_v", "lizard_attn_prefill_noalloc", "lizard_attn_backward",
            "lizard_attn_backward_v", "lizard_gate_projection", "lizard_attn_decode_step", "lizard_attn_decode_step_v",
-           "lizard_check_device_status", "lizard_status_string")
+           "lizard_check_device_status", "lizard_status_string", "lizard_scratch_trim", "lizard_scratch_reserved")
 
 
 class LizardError(RuntimeError):
@@ -95,6 +95,10 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lizard_check_device_status.restype = I
         lib.lizard_status_string.argtypes = [I]
         lib.lizard_status_string.restype = ctypes.c_char_p
+        lib.lizard_scratch_trim.argtypes = [ctypes.c_size_t]
+        lib.lizard_scratch_trim.restype = I
+        lib.lizard_scratch_reserved.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.lizard_scratch_reserved.restype = I
         _lib = lib
         return lib
 
@@ -263,3 +267,16 @@ def lizard_check_device_status(stream=None) -> None:
 
 def lizard_status_string(status: int) -> str:
     return library().lizard_status_string(int(status)).decode()
+
+
+def lizard_scratch_trim(keep_bytes: int = 0) -> None:
+    """Hand the library's scratch on the current device back to the driver,
+    keeping at most ``keep_bytes`` (synchronise earlier calls first)."""
+    _check(library().lizard_scratch_trim(int(keep_bytes)), "lizard_scratch_trim")
+
+
+def lizard_scratch_reserved() -> int:
+    """Bytes the library's scratch pool holds on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(library().lizard_scratch_reserved(ctypes.byref(n)), "lizard_scratch_reserved")
+    return int(n.value)

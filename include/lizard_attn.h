@@ -36,8 +36,10 @@
  *     sequence segments, the backward pass) takes it stream-ordered on
  *     `stream` from a memory pool the library owns (one per device) and
  *     frees it there.  Freed memory stays reserved in that pool for the
- *     library's later calls until the process exits; failure to allocate
- *     is LIZARD_ERR_CUDA (a prefill then runs unsegmented instead).
+ *     library's later calls -- at most the largest scratch of any one call
+ *     so far, e.g. about 810 MB for the backward of B4 H32 L4096 d128 --
+ *     until lizard_scratch_trim returns it or the process exits; failure to
+ *     allocate is LIZARD_ERR_CUDA (a prefill then runs unsegmented instead).
  *   - Supported shapes: d_k == d_v in {64, 128}; 1 <= w <= LIZARD_MAX_WINDOW;
  *     0 <= m <= LIZARD_MAX_META.  Anything else in range but not built is
  *     LIZARD_ERR_UNSUPPORTED; anything meaningless is LIZARD_ERR_INVALID_ARG.
@@ -206,9 +208,10 @@ LIZARD_API lizard_status lizard_attn_prefill_continue_v(const void *q, const voi
  * calls no cudaMalloc, cudaFree or allocating library routine.  A problem
  * whose segment states would not fit (units x (segments - 1) x 66048 bytes)
  * is rejected with LIZARD_ERR_UNSUPPORTED before anything is launched.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on that device.
+ *   - The first call on each device (and the first after a reset of that
+ *     device, which gives it a new context) looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture on that device.
  *   - Every call shares the one array and overwrites what it reads (nothing
  *     in it needs to start at zero), so calls whose work overlaps on the GPU
  *     -- on different streams, or from different host threads -- race and
@@ -220,6 +223,20 @@ LIZARD_API lizard_status lizard_attn_prefill_noalloc(const void *q, const void *
                                           int B, int H, int L, int dk, int dv, int w, int m,
                                           lizard_dtype dtype, void *y, const lizard_state *st,
                                           lizard_stream_t stream);
+
+/*
+ * lizard_scratch_trim: hands the scratch the library's pool holds on the
+ * current device back to the driver, keeping at most `keep_bytes` reserved
+ * for later calls.  Memory of calls still running on the GPU is not
+ * returned: synchronise the streams of earlier calls first.  A device that
+ * never needed scratch has no pool: LIZARD_OK, nothing done.
+ * Not part of the paper's operator; memory management only.
+ */
+LIZARD_API lizard_status lizard_scratch_trim(size_t keep_bytes);
+
+/* lizard_scratch_reserved: bytes the library's scratch pool holds on the
+ * current device (0 without a pool); *bytes must be a host pointer. */
+LIZARD_API lizard_status lizard_scratch_reserved(size_t *bytes);
 
 /*
  * lizard_attn_backward: gradients of a scalar loss through the operator over

@@ -134,7 +134,8 @@ def test_binding_names_match_the_c_abi():
     import hybrid_gated_linear_attn_b300 as pkg
     for name in ("lizard_state_init", "lizard_attn_prefill", "lizard_attn_prefill_continue", "lizard_attn_prefill_noalloc",
                  "lizard_attn_backward", "lizard_gate_projection",
-                 "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string"):
+                 "lizard_attn_decode_step", "lizard_check_device_status", "lizard_status_string",
+                 "lizard_scratch_trim", "lizard_scratch_reserved"):
         assert callable(getattr(pkg, name))
 
 
@@ -224,3 +225,28 @@ def test_valid_variant_on_empty_calls_launches_nothing(lib):
                                      None, v, None) == OK
     assert lib.lizard_attn_prefill_continue_v(None, None, None, None, A, 1.0, 0, 4, None,
                                               ctypes.byref(state()), v, None) == OK
+
+
+def noalloc(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128, dv=128, w=64, m=4,
+            dtype=LA.LIZARD_BF16, y=A, st=None):
+    return lib.lizard_attn_prefill_noalloc(q, k, v, g, mu, alpha, Bn, H, L, dk, dv, w, m, dtype, y,
+                                           ctypes.byref(st) if st is not None else None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    # the allocation-free call covers the bf16, d = 128, w <= 65 prefill only
+    (dict(dtype=LA.LIZARD_F32), UNSUPPORTED), (dict(dk=64, dv=64), UNSUPPORTED), (dict(w=66), UNSUPPORTED),
+    (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
+    (dict(q=None), INVALID), (dict(g=None), INVALID), (dict(y=None), INVALID), (dict(mu=None), INVALID),
+    (dict(v=MIS), INVALID), (dict(y=MIS), INVALID), (dict(dtype=7), INVALID), (dict(w=0), INVALID),
+    (dict(m=-1), INVALID), (dict(L=-1), INVALID), (dict(H=0), INVALID), (dict(Bn=-1), INVALID),
+    (dict(st=state(Bn=3)), INVALID), (dict(st=state(w=32)), INVALID), (dict(st=state(S=None)), INVALID),
+    (dict(st=state(pos=MIS)), INVALID), (dict(st=state(dtype=LA.LIZARD_F32)), INVALID),
+])
+def test_noalloc_rejects(lib, kw, code):
+    assert noalloc(lib, **kw) == code
+
+
+def test_noalloc_empty_calls_launch_nothing(lib):
+    assert noalloc(lib, Bn=0) == OK
+    assert noalloc(lib, q=None, k=None, v=None, g=None, y=None, L=0) == OK  # no state: nothing to reset

@@ -64,3 +64,27 @@ def test_reference_arm_runs_on_rank_zero_only():
     import bench
     args = bench.argparse.Namespace(steps=1, warmup=0, sample_heads=1, gpus=2)
     assert bench.run_reference(args, world=2, rank=1) == 0   # other ranks exit 0 without work
+
+
+def test_bench_gpus_2_launches_two_ranks_by_itself():
+    """A plain ``bench.py --gpus 2`` (no launcher) runs two ranks under
+    torch.distributed.run; the measured step is replaced by a CPU stand-in
+    (tests/bench_stub_main.py), so this checks the launch, the gloo group
+    and the max over ranks."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_PORT")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "bench_stub_main.py"), "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [json.loads(x) for x in out.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    assert lines[0]["n_gpus"] == 2 and lines[0]["ms_per_step"] == 2.0
+
+
+def test_bench_refuses_a_world_size_other_than_gpus():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "bench_stub_main.py"), "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 2 and "WORLD_SIZE=1" in out.stderr

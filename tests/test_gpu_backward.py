@@ -39,6 +39,18 @@ def _gpu_backward(inp, w):
     return [None if t is None else t.cpu() for t in out]
 
 
+def _dalpha_error(inp, w, got: float, ref: float) -> float:
+    """Error of d alpha = sum_t dy_t . ya_t relative to |d alpha|.  The
+    sum has B H L d_v terms of both signs; its rounding errors are
+    independent per term, so their natural scale is the L2 norm of the
+    terms, ||dy * ya||_2, which is also the typical size of |d alpha| for a
+    random dy.  When a seed makes the sum cancel to below 1/20 of that size
+    the relative error is measured against that size instead."""
+    _, _, ya = O.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], w, branches=True)
+    scale = float((inp["dy"].double() * ya).norm())
+    return abs(got - ref) / max(abs(ref), scale / 20.0, 1e-30)
+
+
 def _check(inp, w):
     dq, dk, dv, dg, dmu, dal = _gpu_backward(inp, w)
     ref = O.backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], w, inp["dy"].double())
@@ -59,11 +71,7 @@ def _check(inp, w):
             errs["dmu"] = rel_l2(dmu, ref["dmu"])
         else:  # alpha = 0: the sinks get no gradient at all
             errs["dmu"] = 0.0 if float(dmu.abs().max()) == 0.0 else float("inf")
-    # d alpha = sum_t dy_t . ya_t: a sum of terms of both signs, each computed
-    # to relative accuracy tol, so its error is bounded by tol * sum |dy ya|.
-    _, _, ya = O.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], w, branches=True)
-    scale = float((inp["dy"].double() * ya).abs().sum())
-    errs["dalpha"] = abs(float(dal) - float(ref["dalpha"])) / max(scale, 1e-30)
+    errs["dalpha"] = _dalpha_error(inp, w, float(dal), float(ref["dalpha"]))
     bad = {n: e for n, e in errs.items() if not e <= tol}
     assert not bad, f"rel L2 above {tol}: {bad} (all: {errs})"
     return errs
@@ -114,59 +122,29 @@ def test_empty_sequence_gives_zero_parameter_gradients():
     assert dq.numel() == 0 and float(dal) == 0.0 and torch.all(dmu == 0)
 
 
-def test_llama3_8b_full_size_sampled_heads():
-    """B4 H32 L4096 d128 bf16 in one launch; oracle on 3 sampled heads
-    (dq, dk, dv, dg of those units)."""
-    wl = WORKLOADS["llama3_8b"]
+def _full_size(wl_name, seed):
+    """One launch at the workload's full size; the oracle backward on every
+    (batch, head) unit (one thread per unit); every gradient compared over
+    all elements."""
+    wl = WORKLOADS[wl_name]
     inp = prefill_inputs(wl)
-    gen = torch.Generator().manual_seed(99)
+    gen = torch.Generator().manual_seed(seed)
     inp["dy"] = torch.randn(wl.B, wl.H, wl.L, wl.dv, generator=gen).to(inp["q"].dtype)
-    dq, dk, dv, dg, _, _ = _gpu_backward(inp, wl.w)
-    units = [(0, 0), (1, 17), (3, 31)]
-    import threading
-    refs = [None] * len(units)
-
-    def run(i, b, h):
-        sl = {n: inp[n][b, h][None, None] for n in ("q", "k", "v", "g", "dy")}
-        refs[i] = O.backward(sl["q"], sl["k"], sl["v"], sl["g"], inp["mu"][h:h + 1], wl.alpha, wl.w,
-                             sl["dy"].double(), threads=1)
-
-    ths = [threading.Thread(target=run, args=(i, b, h)) for i, (b, h) in enumerate(units)]
-    for t in ths:
-        t.start()
-    for t in ths:
-        t.join()
-    for name, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg)):
-        g_s = torch.stack([got[b, h] for (b, h) in units])
-        r_s = torch.stack([r[name][0, 0] for r in refs])
-        err = rel_l2(g_s, r_s)
-        assert err <= TOL[torch.bfloat16], f"{name}: rel L2 {err:.3e}"
+    dq, dk, dv, dg, dmu, dal = _gpu_backward(inp, wl.w)
+    ref = O.backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], wl.alpha, wl.w, inp["dy"].double())
+    tol = TOL[torch.bfloat16]
+    errs = {n: rel_l2(got, ref[n]) for n, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dmu", dmu))}
+    errs["dalpha"] = _dalpha_error(inp, wl.w, float(dal), float(ref["dalpha"]))
+    bad = {n: e for n, e in errs.items() if not e <= tol}
+    assert not bad, f"{wl_name}: above {tol}: {bad} (all: {errs})"
 
 
-def test_decay_stress_full_size_sampled_heads():
-    """B2 H32 L8192 d128 bf16, g ~ N(0, 2), w128 m8 alpha 0.5 (the exact
-    CUDA-core path: w > 65) in one launch; oracle on 3 sampled heads."""
-    wl = WORKLOADS["decay_stress"]
-    inp = prefill_inputs(wl)
-    gen = torch.Generator().manual_seed(98)
-    inp["dy"] = torch.randn(wl.B, wl.H, wl.L, wl.dv, generator=gen).to(inp["q"].dtype)
-    dq, dk, dv, dg, _, _ = _gpu_backward(inp, wl.w)
-    units = [(0, 3), (1, 0), (1, 30)]
-    import threading
-    refs = [None] * len(units)
+def test_llama3_8b_full_size_all_units():
+    """B4 H32 L4096 d128 bf16 (tensor-core path), all 128 units."""
+    _full_size("llama3_8b", 99)
 
-    def run(i, b, h):
-        sl = {n: inp[n][b, h][None, None] for n in ("q", "k", "v", "g", "dy")}
-        refs[i] = O.backward(sl["q"], sl["k"], sl["v"], sl["g"], inp["mu"][h:h + 1], wl.alpha, wl.w,
-                             sl["dy"].double(), threads=1)
 
-    ths = [threading.Thread(target=run, args=(i, b, h)) for i, (b, h) in enumerate(units)]
-    for t in ths:
-        t.start()
-    for t in ths:
-        t.join()
-    for name, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg)):
-        g_s = torch.stack([got[b, h] for (b, h) in units])
-        r_s = torch.stack([r[name][0, 0] for r in refs])
-        err = rel_l2(g_s, r_s)
-        assert err <= TOL[torch.bfloat16], f"{name}: rel L2 {err:.3e}"
+def test_decay_stress_full_size_all_units():
+    """B2 H32 L8192 d128 bf16, g ~ N(0, 2), w128 m8 alpha 0.5 (w > 65: the
+    exact CUDA-core path), all 64 units."""
+    _full_size("decay_stress", 98)

@@ -20,28 +20,26 @@ from hybrid_gated_linear_attn_b300.inputs import WORKLOADS, prefill_inputs, rel_
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-2  # the bf16 parity tolerance of the other GPU tests
-
-
 def test_prefill_noalloc_matches_prefill_on_two_calls():
     B.build()
     # Two (batch, head) units and 47 chunks: the prompt runs as 5 sequence
-    # segments, whose start states go through the scratch array.
-    wl = WORKLOADS["llama3_8b"].replace(B=1, H=2, L=3000, w=48, seed=123)
-    inp = prefill_inputs(wl)
-    q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
-    st_ref = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
-    y_ref = lizard_attn_prefill(q, k, v, g, mu, wl.alpha, wl.w, state=st_ref)
-    lizard_check_device_status()
-    assert torch.isfinite(y_ref.float()).all() and float(y_ref.float().abs().max()) > 0
-    for call in range(2):
+    # segments, whose start states go through the scratch array.  The two
+    # calls use different inputs, so that anything left in the array by the
+    # first call would show in the second.  Both entry points run the same
+    # kernels with the same segment count, so the results are bit-identical.
+    for call, seed in enumerate((123, 456)):
+        wl = WORKLOADS["llama3_8b"].replace(B=1, H=2, L=3000, w=48, seed=seed)
+        inp = prefill_inputs(wl)
+        q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
+        st_ref = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
+        y_ref = lizard_attn_prefill(q, k, v, g, mu, wl.alpha, wl.w, state=st_ref)
+        lizard_check_device_status()
+        assert torch.isfinite(y_ref.float()).all() and float(y_ref.float().abs().max()) > 0
         st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
         y = torch.full_like(y_ref, float("nan"))
         lizard_attn_prefill_noalloc(q, k, v, g, mu, wl.alpha, wl.w, y=y, state=st)
         lizard_check_device_status()
-        err = rel_l2(y.cpu(), y_ref.cpu())
-        assert err <= TOL, f"call {call}: rel L2 {err:.3e}"
-        errS = rel_l2(st.S.cpu(), st_ref.S.cpu())
-        assert errS <= TOL, f"call {call}: state rel L2 {errS:.3e}"
+        assert torch.equal(y.cpu(), y_ref.cpu()), f"call {call}: rel L2 {rel_l2(y.cpu(), y_ref.cpu()):.3e}"
+        assert torch.equal(st.S.cpu(), st_ref.S.cpu()), f"call {call}: state differs"
         assert torch.equal(st.ring_k.cpu(), st_ref.ring_k.cpu()) and torch.equal(st.ring_v.cpu(), st_ref.ring_v.cpu())
         assert torch.equal(st.pos.cpu(), st_ref.pos.cpu())
