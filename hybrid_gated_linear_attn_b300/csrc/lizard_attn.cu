@@ -163,26 +163,6 @@ static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
-{
-    const int units = pa.B * pa.H, kv_units = pa.B * (pa.H / pa.group);
-    CUtensorMap tq, tk, tv;
-    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
-        !make_token_map(&tv, pa.v, kv_units, pa.L))
-        return LIZARD_ERR_CUDA;
-    tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
-                  static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
-                  static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
-                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
-                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0, pa.alpha_h, pa.group};
-    auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
-                                                                          : tc::prefill_tc_kernel<2>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) != cudaSuccess)
-        return LIZARD_ERR_CUDA;
-    kern<<<units, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
-    return launch_status();
-}
-
 template <int NP>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                           const ws::WsArgs &wa, int ctas, cudaStream_t s)
@@ -240,6 +220,54 @@ static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensor
     if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
     seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, units, nseg, sc);
     return launch_status();
+}
+
+// Lock-step tensor-core prefill (bf16, d = 128, 66 <= w <= 129).  Like the
+// warp-specialised one, a prompt from the empty state with few (batch, head)
+// units runs as sequence segments after the segment pre-pass; a continued
+// prompt runs unsegmented.
+static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
+{
+    const int units = pa.B * pa.H, kv_units = pa.B * (pa.H / pa.group);
+    const int nchunks = (pa.L + tc::C - 1) / tc::C;
+    int nseg = pa.cont ? 1 : prefill_segments(units, nchunks);
+    if (nseg > nchunks) nseg = nchunks;
+    const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
+    nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
+    if (nseg < 1) nseg = 1;
+    CUtensorMap tq, tk, tv, tg;
+    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
+        !make_token_map(&tv, pa.v, kv_units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
+        return LIZARD_ERR_CUDA;
+    float *seg_states = nullptr;
+    if (nseg > 1 && scratch_alloc(reinterpret_cast<void **>(&seg_states), segment_states_bytes(units, nseg), s) !=
+                        cudaSuccess) {
+        cudaGetLastError();
+        nseg = 1;  // no scratch to be had: one CTA per unit walks the whole prompt
+    }
+    lizard_status rc = LIZARD_OK;
+    if (nseg > 1)
+        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, seg::ScanCont{}, pa.H,
+                                   pa.group, s);
+    tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
+                  static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
+                  static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
+                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
+                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0, pa.alpha_h, pa.group,
+                  seg_states, nseg > 1 ? seg_chunks : nchunks, nseg};
+    auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
+                                                                          : tc::prefill_tc_kernel<2>;
+    if (rc == LIZARD_OK) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) !=
+            cudaSuccess)
+            rc = LIZARD_ERR_CUDA;
+        else {
+            kern<<<units * nseg, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
+            rc = launch_status();
+        }
+    }
+    if (seg_states && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
+    return rc;
 }
 
 // Warp-specialised tensor-core prefill (bf16, d = 128, w <= 65).  With few

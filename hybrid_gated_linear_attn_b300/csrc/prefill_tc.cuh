@@ -97,6 +97,12 @@ struct TcArgs {
     const float *S0;
     const float *alpha_h;  // per-head anchor weights (null: alpha)
     int group;             // query heads per key/value head (maps tk, tv over B x H / group heads)
+    // Sequence segments (a prompt from the empty state only): CTA (unit,
+    // seg) covers chunks [seg*seg_chunks, (seg+1)*seg_chunks) and starts
+    // from S_init[unit][seg-1] (row = key dim), the state after the earlier
+    // segments; its band reaches NP chunks back into the previous segment.
+    const float *S_init;
+    int seg_chunks, nseg;
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -153,13 +159,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
-    const int unit = blockIdx.x, h = unit % a.H;
+    const int nseg = a.nseg;
+    const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, h = unit % a.H;
     const int L = a.L, w = a.w, m = a.m;
     const int nchunks = (L + C - 1) / C;
+    const int c_begin = seg * a.seg_chunks, c_end = min(nchunks, c_begin + a.seg_chunks);
+    const bool last_seg = seg == nseg - 1;
     // Window history of a continued prompt: NH chunks before the prompt
-    // (chunks -NH .. -1), of which tokens -nvalid .. -1 are keys.  Chunk c
-    // lives in k/v slot (c + NH) % NR.
+    // (chunks -NH .. -1), of which tokens -nvalid .. -1 are keys.  A later
+    // segment's band starts NP chunks into the previous segment.  Chunk c
+    // lives in k/v slot (c - c_begin + NPRE) % NR.
     const int NH = a.cont ? NP : 0;
+    const int NPRE = seg > 0 ? NP : NH;
+    const int c_lo = c_begin - NPRE;  // first chunk of the first band
+    auto slot_of = [&](int c) { return (c - c_lo) % NR; };
     const int kvu = kv_unit(unit, a.H, a.group);  // this head's key/value head
     // Prep mapping: key dims 2ip and 2ip+1, tokens 16*tqr .. 16*tqr+15.
     const int ip = tid & 63, tqr = tid >> 6;
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
-        *p0_slot = a.cont ? take_start_position(a.pos + unit / a.H, a.H, L) : 0;
+        *p0_slot = a.cont ? take_start_position(a.pos + unit / a.H, a.H * nseg, L) : 0;
     }
     // Meta keys of this head, zero rows past m.
     for (int e = tid; e < META_ROWS * D; e += THREADS) {
@@ -208,9 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         fence_proxy_async_smem();
     }
-    if (warp < 4) {  // S^T = S0^T (zero when not given)
+    if (warp < 4) {  // S^T = the state after the earlier segments, or S0 (zero when not given)
         const int j = 32 * quarter + lane;
-        const float *Si = a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr;
+        const float *Si = seg > 0 ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * D * D + j
+                                  : (a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr);
         for (int c = 0; c < D; c += 16) {
             uint32_t z[16];
 #pragma unroll
@@ -243,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++issued[B_Q];
     };
     auto issue_kv = [&](int c) {
-        const int s = (c + NH) % NR;
+        const int s = slot_of(c);
         uint8_t *base = sm + OFF_KV + s * KV_SLOT;
         mbar_arrive_expect_tx(&bar_kv[s], 4 * TILE);
         tma_load_3d(base, &tk, &bar_kv[s], 0, c * C, kvu);
@@ -252,10 +266,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(base + V_OFF + TILE, &tv, &bar_kv[s], 64, c * C, kvu);
         ++issued[B_KV + s];
     };
-    if (tid == 0 && nchunks > 0) {
-        issue_q(0);
-        issue_kv(0);
-        if (nchunks > 1) issue_kv(1);
+    if (tid == 0 && c_end > c_begin) {
+        if (seg > 0)
+            for (int c = c_lo; c < c_begin; ++c) issue_kv(c);  // the previous segment's band chunks
+        issue_q(c_begin);
+        issue_kv(c_begin);
+        if (c_begin + 1 < c_end) issue_kv(c_begin + 1);
     }
 
     // Gate logits of this thread's two key dims for its 16 tokens, one chunk
@@ -269,19 +285,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             gnext[tt] = tg < L ? gp[(size_t)tg * (D / 2)] : 0x7F807F80u;
         }
     };
-    if (nchunks > 0) load_g(0);
+    if (c_end > c_begin) load_g(c_begin);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     bool aborted = false;
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
         const int c0 = c * C, n = min(C, L - c0);
-        const uint32_t slot_off = OFF_KV + ((c + NH) % NR) * KV_SLOT;
+        const uint32_t slot_off = OFF_KV + slot_of(c) * KV_SLOT;
 
         // ---- P1: this chunk's tiles, and the previous state update done ----
-        bool ok = wait_bar(B_Q) && wait_bar(B_KV + (c + NH) % NR);
-        if (c > 0) ok = ok && wait_bar(B_ST);
+        bool ok = wait_bar(B_Q) && wait_bar(B_KV + slot_of(c));
+        if (c == c_begin && seg > 0)
+            for (int cp = c_lo; cp < c_begin; ++cp) ok = ok && wait_bar(B_KV + slot_of(cp));
+        if (c > c_begin) ok = ok && wait_bar(B_ST);
         if (__syncthreads_or(!ok)) { aborted = true; break; }
         tc_fence_after();
         if (tid == 0) {  // window + meta logits
@@ -295,8 +313,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
-                if (cj < -NH) continue;
-                const uint32_t kb = sb + OFF_KV + ((cj + NH) % NR) * KV_SLOT;
+                if (cj < c_lo) continue;
+                const uint32_t kb = sb + OFF_KV + slot_of(cj) * KV_SLOT;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t ad = smem_desc(sb + OFF_Q + (kk / 4) * TILE + (kk % 4) * 32, 16, 1024);
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             dec[2 * ip] = ex2(l2a);
             dec[2 * ip + 1] = ex2(l2b);
         }
-        if (c + 1 < nchunks) load_g(c + 1);
+        if (c + 1 < c_end) load_g(c + 1);
 
         float q0a[16], q0b[16];
         {
@@ -437,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
 
         // ---- P4: next q tile; q*e^{b} operand and y^T part 1; softmax -> W ----
-        if (tid == 0 && c + 1 < nchunks) {
+        if (tid == 0 && c + 1 < c_end) {
             fence_proxy_async_smem();
             issue_q(c + 1);
         }
@@ -548,8 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j <= NP; ++j) {
                 const int cj = c - NP + j;
-                if (cj < -NH) continue;
-                const uint32_t vb = sb + OFF_KV + ((cj + NH) % NR) * KV_SLOT + V_OFF;
+                if (cj < c_lo) continue;
+                const uint32_t vb = sb + OFF_KV + slot_of(cj) * KV_SLOT + V_OFF;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t ad = smem_desc(vb + kk * 2048, 8192, 1024);
@@ -565,7 +583,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 
         // ---- P6: k/v prefetch; decay of S^T; output ----
-        if (tid == 0 && c + 2 < nchunks) {
+        if (tid == 0 && c + 2 < c_end) {
             fence_proxy_async_smem();
             issue_kv(c + 2);
         }
@@ -618,7 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---- final state ----
-    if (!aborted && nchunks > 0) {
+    if (!aborted && c_end > c_begin) {
         const bool ok = wait_bar(B_ST);
         if (__syncthreads_or(!ok)) aborted = true;
     }
@@ -632,7 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 while (done[b] < issued[b] && wait_bar((int)b)) {
                 }
         }
-    } else if (a.S_out) {
+    } else if (a.S_out && last_seg) {
         if (warp < 4) {
             const int j = 32 * quarter + lane;
             float *So = a.S_out + (size_t)unit * D * D + j;

@@ -70,6 +70,10 @@ CASES = [
     ("segments_exact_intra", "bf16", 1, 1, 1500, 128, 32, 2, -8.0, 4.0, 1.0),
     ("segments_window_one", "bf16", 1, 2, 1200, 128, 1, 3, 3.0, 1.0, 1.0),
     ("segments_open_gates_no_meta", "bf16", 1, 1, 2500, 128, 64, 0, 12.0, 0.5, 1.0),
+    # windows above 65 (three-chunk band) as sequence segments
+    ("segments_w100", "bf16", 1, 2, 2000, 128, 100, 4, 3.0, 1.0, 1.0),
+    ("segments_w128_strong_decay", "bf16", 1, 2, 2100, 128, 128, 8, 0.0, 2.0, 0.5),
+    ("segments_w66_exact_intra", "bf16", 1, 1, 1500, 128, 66, 2, -8.0, 4.0, 1.0),
 ]
 
 
