@@ -840,14 +840,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t *qr_t = sm + SM::OP + b * OPB + kblk * KB_T, *kr_t = qr_t + 2 * KB_T;
             float *vb = vec + b * NVEC * 128;
             if (!unsafe) {
-                auto emit = [&](int tt, float2 qs2, float2 ks2) {
-                    const uint32_t off = sw128_offset(16 * hq + tt, kbyte);
-                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
-                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
-                    const float2 kr = mul2(kv, ks2), qr = mul2(qv, qs2);
-                    *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
-                    *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
-                };
                 // Z_t = 2^{r - b_t}: a running product of iv from the start
                 // of the thread's half, times 2^r in the first half
                 // (2^{r - b_t} = 2^r prod_{0..t} iv there).  KR = k Z,
