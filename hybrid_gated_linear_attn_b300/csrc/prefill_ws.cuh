@@ -136,11 +136,11 @@ struct WsArgs {
 // Optional clock trace of CTA 0 (compiled with -DLIZARD_TRACE): one clock64
 // stamp per (chunk, event), read by lizard_debug_trace.
 #ifdef LIZARD_TRACE
-constexpr int TRACE_CHUNKS = 64, TRACE_EVENTS = 24;
+constexpr int TRACE_CHUNKS = 64, TRACE_EVENTS = 32;
 __device__ unsigned long long g_ws_trace[TRACE_CHUNKS][TRACE_EVENTS];
 #define LZ_TRACE(pc, ev)                                                              \
     do {                                                                              \
-        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (pc) < TRACE_CHUNKS) g_ws_trace[(pc)][(ev)] = clock64(); \
+        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (pc) < TRACE_CHUNKS && (ev) < TRACE_EVENTS) g_ws_trace[(pc)][(ev)] = clock64(); \
     } while (0)
 #else
 #define LZ_TRACE(pc, ev) \
@@ -529,6 +529,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if ((pc == 0 && c_lo < c_begin && !bwait(&k_full[0], 0, abort_f)) ||
                     !bwait(&k_full[s], r / NR, abort_f) || !bwait(&q_full[qs], pc / QS, abort_f) ||
                     (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) { give_up(); break; }
+                LZ_TRACE(pc, 24);
                 tc_fence_after();
                 // window + meta logits
 #pragma unroll 1
@@ -581,6 +582,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 LZ_TRACE(pc, 4);
                 mbar_arrive(&k_empty[s]);  // the prep of this chunk has read its raw keys
                 if (!bwait(s_ready, pc, abort_f) || !bwait(&v_full[s], r / NR, abort_f)) { give_up(); break; }
+                LZ_TRACE(pc, 26);
                 tc_fence_after();
                 // Shat^T += V^T K, K = KR (KL for an unsafe chunk)
                 const uint32_t vb = sb + SM::KV + s * SLOT + SLOT_V, kb = sb + SM::OP + b * OPB + 2 * KB_T;
@@ -605,6 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // y^T = S16 QR^T (inter-chunk readout)
                 if (!bwait(&op_full[b], pc >> 1, abort_f) || !bwait(s_ready, pc, abort_f) ||
                     (pc >= 1 && !bwait(y_free, pc - 1, abort_f))) { give_up(); break; }
+                LZ_TRACE(pc, 27);
                 tc_fence_after();
                 const uint32_t ob = sb + SM::OP + b * OPB;
                 {
@@ -620,6 +623,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // y^T += V_band^T W^T
                 if (!bwait(w_full, pc, abort_f) || !bwait(&v_full[r % NR], r / NR, abort_f) ||
                     (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f))) { give_up(); break; }
+                LZ_TRACE(pc, 25);
                 tc_fence_after();
 #pragma unroll 1
                 for (int j = 0; j <= NP; ++j) {
