@@ -369,7 +369,7 @@ def run_ours(args, world, rank, local):
 
         # ---- the decay-stress and long-context prefill workloads, same run ----
         extra = {}
-        for name in ("decay_stress", "long_context"):
+        for name in ("decay_stress", "long_context", "d64"):
             xwl = WORKLOADS[name]
             xin = prefill_inputs(xwl, seed=rank_seed(xwl.seed, rank))
             xq, xk, xv, xg, xmu = (xin[n].cuda() for n in ("q", "k", "v", "g", "mu"))

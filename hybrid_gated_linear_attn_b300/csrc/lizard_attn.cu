@@ -1,10 +1,10 @@
 // lizard_attn.cu -- C ABI of the Lizard hybrid attention operator.
 //
 // Host-side validation and launch of the kernels in decode.cuh,
-// prefill_ws.cuh (bf16, d = 128, w <= 65: warp-specialised tensor cores, with
-// the segment pre-pass of prefill_state.cuh), prefill_tc.cuh (bf16, d = 128,
-// w > 65: tensor cores), prefill_simt.cuh (fp32 and d = 64: CUDA cores, exact
-// fp32), prefill_cont.cuh (start position of a continued prompt),
+// prefill_ws.cuh (bf16, d = 128 or 64, w <= 65: warp-specialised tensor
+// cores, with the segment pre-pass of prefill_state.cuh for d = 128),
+// prefill_tc.cuh (bf16, d = 128, w > 65: tensor cores), prefill_simt.cuh
+// (fp32, and bf16 d = 64 with w > 65: CUDA cores, exact fp32), prefill_cont.cuh (start position of a continued prompt),
 // backward_simt.cuh / backward_tc.cuh (gradients), gate_proj.cuh (the gate
 // projection) and the state initialiser below.  Declarations and the contract of every entry point are
 // in include/lizard_attn.h.
@@ -148,14 +148,14 @@ static encode_tiled_fn tensor_map_encoder()
     return fn;
 }
 
-// [units][L][128] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128B swizzle,
-// rows past L read as zero.
-static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
+// [units][L][d] bf16 (d = 128 or 64) viewed as a 3-D tensor; 64 x 64 boxes,
+// 128B swizzle, rows past L read as zero.
+static bool make_token_map(CUtensorMap *map, const void *base, int units, int L, int d = 128)
 {
     encode_tiled_fn enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)L, (cuuint64_t)units};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)L * 128 * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)units};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -163,11 +163,11 @@ static bool make_token_map(CUtensorMap *map, const void *base, int units, int L)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NP>
+template <int NP, int DH>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                           const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
-    auto kern = ws::prefill_ws_kernel<NP>;
+    auto kern = ws::prefill_ws_kernel<NP, DH>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
@@ -270,25 +270,26 @@ static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
     return rc;
 }
 
-// Warp-specialised tensor-core prefill (bf16, d = 128, w <= 65).  With few
-// (batch, head) units and a long prompt the sequence is split into segments
-// that run side by side, after a pre-pass that computes every segment's
-// start state; `scratch` (nullable) holds those states, else they live in
-// stream-ordered scratch from the library's pool (freed on `s`).
+// Warp-specialised tensor-core prefill (bf16, d = 128 or 64, w <= 65).  With
+// few (batch, head) units and a long prompt the sequence (d = 128) is split
+// into segments that run side by side, after a pre-pass that computes every
+// segment's start state; `scratch` (nullable) holds those states, else they
+// live in stream-ordered scratch from the library's pool (freed on `s`).
+// d = 64 runs one CTA per unit on the same tiles, zero-padded.
 static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, float *scratch = nullptr,
-                                       size_t scratch_bytes = 0, int force_segments = 0)
+                                       size_t scratch_bytes = 0, int force_segments = 0, int d = 128)
 {
     const int units = pa.B * pa.H;
     const int nchunks = (pa.L + ws::C - 1) / ws::C;
-    int nseg = force_segments > 0 ? force_segments : prefill_segments(units, nchunks);
+    int nseg = d != ws::D ? 1 : force_segments > 0 ? force_segments : prefill_segments(units, nchunks);
     if (nseg > nchunks) nseg = nchunks;
     const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
     nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
     if (nseg < 1) nseg = 1;
     const int kv_units = pa.B * (pa.H / pa.group);
     CUtensorMap tq, tk, tv, tg;
-    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
-        !make_token_map(&tv, pa.v, kv_units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
+    if (!make_token_map(&tq, pa.q, units, pa.L, d) || !make_token_map(&tk, pa.k, kv_units, pa.L, d) ||
+        !make_token_map(&tv, pa.v, kv_units, pa.L, d) || !make_token_map(&tg, pa.g, units, pa.L, d))
         return LIZARD_ERR_CUDA;
     float *seg_states = nullptr;
     bool owned = false;
@@ -330,8 +331,10 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
                   nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg,
                   pa.cont, seg0_state, hist, pa.alpha_h, pa.group};
     if (rc == LIZARD_OK)
-        rc = pa.w == 1 ? launch_prefill_ws_np<0>(tq, tk, tv, wa, units * nseg, s)
-                       : launch_prefill_ws_np<1>(tq, tk, tv, wa, units * nseg, s);
+        rc = d == ws::D ? (pa.w == 1 ? launch_prefill_ws_np<0, ws::D>(tq, tk, tv, wa, units * nseg, s)
+                                     : launch_prefill_ws_np<1, ws::D>(tq, tk, tv, wa, units * nseg, s))
+                        : (pa.w == 1 ? launch_prefill_ws_np<0, 64>(tq, tk, tv, wa, units * nseg, s)
+                                     : launch_prefill_ws_np<1, 64>(tq, tk, tv, wa, units * nseg, s));
     if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -668,7 +671,7 @@ lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v,
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == LIZARD_BF16)
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
-                         : launch_prefill<__nv_bfloat16, 64>(pa, s);
+                         : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 
@@ -740,7 +743,7 @@ lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
         return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
-                         : launch_prefill<__nv_bfloat16, 64>(pa, s);
+                         : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 

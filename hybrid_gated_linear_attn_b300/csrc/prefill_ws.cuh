@@ -1,5 +1,5 @@
 // prefill_ws.cuh -- chunked Lizard prefill on tcgen05 tensor cores as a
-// warp-specialised pipeline (bf16 inputs, d = 128, window w <= 65).
+// warp-specialised pipeline (bf16 inputs, d = 128 or 64, window w <= 65).
 //
 // Operator: gated linear attention (Lizard, gist.science/de section 2 item 1)
 // + anchor window with meta-memory sinks (item 2) + alpha combine (item 3).
@@ -47,6 +47,12 @@
 //   warps 16-19  window softmax: W from SC and A
 // Every hand-off is an mbarrier; every wait is bounded (a timeout records
 // DEV_TIMEOUT, drains the copies and products in flight, and returns).
+//
+// Head dim d = 64 runs on the same tiles, 128 wide: the key/value dims
+// 64..127 of every shared-memory tile are zero (cleared at set-up; the TMA
+// loads only the first 64-dim box), so the state's extra rows and columns
+// stay zero.  Products over the key dim (scores, A, the readout) take d / 16
+// K-steps; the gate prep and the state pass skip the padding.
 #pragma once
 
 #include "common.cuh"
@@ -121,9 +127,9 @@ struct WsArgs {
     // Continuation of a sequence (0 / null for a prompt from the empty
     // state): with cont = 1 every CTA takes the start position from pos
     // (take_start_position) and the first segment sees the window history
-    // as chunk -1: from `hist` ([units][2][64][D], keys then values, row r =
+    // as chunk -1: from `hist` ([units][2][64][d], keys then values, row r =
     // token r - 64, zero where no key) when given, else from the ring, which
-    // the CTA then writes only at its end (one segment).  S0 [units][D][D] is
+    // the CTA then writes only at its end (one segment).  S0 [units][d][d] is
     // the start state of the first segment (may be S_out when there is one
     // segment: it is read before S_out is written).
     int cont;
@@ -331,7 +337,7 @@ __device__ __forceinline__ void mma_chain(uint32_t d, uint64_t da, uint64_t db, 
     }
 }
 
-template <int NP>
+template <int NP, int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const WsArgs a)
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nseg = a.nseg;
     const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, h = unit % a.H;
     const int L = a.L, w = a.w, m = a.m;
+    constexpr int d = DH, nbox = d / 64, nk = d / 16;  // head dim; 64-dim boxes per tile, K-steps over the key dim
     const int nchunks = (L + C - 1) / C;
     // This CTA's chunks, and the first chunk it loads: the band of its first
     // chunk reaches NP chunks back into the previous segment, or into the
@@ -412,17 +419,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t p0 = a.cont ? *p0_slot : 0;
     const int kvu = kv_unit(unit, a.H, a.group);  // this head's key/value head
     const int nvalid = a.cont ? (int)min(p0, (int64_t)(w - 1)) : 0;
+    if constexpr (d < D) {
+        // the padding dims of the k/v ring, the q stages and the operand buffers
+        for (uint32_t e = tid; e < SM::W / 16; e += THREADS)
+            *reinterpret_cast<uint4 *>(sm + 16 * e) = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+    }
     if (c_lo < 0) {
         // Window history (chunk -1) into k/v slot 0, zero rows where no key,
         // in the swizzled layout of a TMA-loaded tile.
-        const __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
-        const __nv_bfloat16 *hk = a.hist ? a.hist + (size_t)unit * 2 * C * D : nullptr;
-        const __nv_bfloat16 *hv = a.hist ? hk + C * D : nullptr;
+        const __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * d, *rv = a.ring_v + (size_t)unit * w * d;
+        const __nv_bfloat16 *hk = a.hist ? a.hist + (size_t)unit * 2 * C * d : nullptr;
+        const __nv_bfloat16 *hv = a.hist ? hk + C * d : nullptr;
         const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        for (int e = tid; e < C * (D / 8); e += THREADS) {
-            const int r = e / (D / 8), i8 = (e % (D / 8)) * 8;
-            const __nv_bfloat16 *kr = hk ? hk + (size_t)r * D : history_row(rk, p0, r - C, nvalid, w, D);
-            const __nv_bfloat16 *vr = hk ? hv + (size_t)r * D : history_row(rv, p0, r - C, nvalid, w, D);
+        for (int e = tid; e < C * (d / 8); e += THREADS) {
+            const int r = e / (d / 8), i8 = (e % (d / 8)) * 8;
+            const __nv_bfloat16 *kr = hk ? hk + (size_t)r * d : history_row(rk, p0, r - C, nvalid, w, d);
+            const __nv_bfloat16 *vr = hk ? hv + (size_t)r * d : history_row(rv, p0, r - C, nvalid, w, d);
             const uint32_t sw = sw128_offset(r, (i8 % 64) * 2);
             *reinterpret_cast<uint4 *>(sm + SM::KV + (i8 / 64) * KB_K + sw) =
                 kr ? *reinterpret_cast<const uint4 *>(kr + i8) : zero;
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = e / (META_ROWS * 64), rem = e % (META_ROWS * 64), r = rem / 64, ip = rem % 64;
         const int i = 2 * ip;
         uint32_t val = 0u;
-        if (r < m) val = *reinterpret_cast<const uint32_t *>(a.mu + ((size_t)h * m + r) * D + i);
+        if (r < m && i < d) val = *reinterpret_cast<const uint32_t *>(a.mu + ((size_t)h * m + r) * d + i);
         *reinterpret_cast<uint32_t *>(sm + SM::KV + s * SLOT + (i / 64) * KB_K +
                                       sw128_offset(C + r, (i % 64) * 2)) = val;
     }
@@ -461,9 +474,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             // bulk prefetch two chunks ahead keeps them in L2.
             auto prefetch_g = [&](int c) {
                 const int n = min(C, L - c * C);
-                prefetch_l2(a.g + ((size_t)unit * L + (size_t)c * C) * D, (uint32_t)n * D * 2u);
+                prefetch_l2(a.g + ((size_t)unit * L + (size_t)c * C) * d, (uint32_t)n * d * 2u);
             };
             for (int c = c_begin; c < min(c_end, c_begin + 2); ++c) prefetch_g(c);
+            // One 64-token tile: nbox boxes of 64 dims, `blk` bytes apart.
+            auto load_tile = [&](uint8_t *dst, uint32_t blk, const CUtensorMap *map, uint64_t *bar, int c, int u) {
+                mbar_arrive_expect_tx(bar, nbox * KB_T);
+                for (int x = 0; x < nbox; ++x) tma_load_3d(dst + x * blk, map, bar, 64 * x, c * C, u);
+            };
             // keys and values of the band chunks before this segment; the
             // window history (chunk -1) is in place since the set-up
             for (int c = c_lo; c < c_begin; ++c) {
@@ -473,12 +491,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive(&k_full[s]);
                     mbar_arrive(&v_full[s]);
                 } else {
-                    mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                    tma_load_3d(base, &tk, &k_full[s], 0, c * C, kvu);
-                    tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, kvu);
-                    mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                    tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, kvu);
-                    tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, kvu);
+                    load_tile(base, KB_K, &tk, &k_full[s], c, kvu);
+                    load_tile(base + SLOT_V, KB_T, &tv, &v_full[s], c, kvu);
                 }
                 ++k_issued[s];
                 ++v_issued[s];
@@ -489,22 +503,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int s = r % NR;
                 uint8_t *base = sm + SM::KV + s * SLOT;
                 if (r >= NR && !bwait(&k_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
-                mbar_arrive_expect_tx(&k_full[s], 2 * KB_T);
-                tma_load_3d(base, &tk, &k_full[s], 0, c * C, kvu);
-                tma_load_3d(base + KB_K, &tk, &k_full[s], 64, c * C, kvu);
+                load_tile(base, KB_K, &tk, &k_full[s], c, kvu);
                 ++k_issued[s];
                 LZ_TRACE(pc, 15);
                 const int qs = pc % QS;
                 if (pc >= QS && !bwait(&q_empty[qs], pc / QS - 1, abort_f)) { give_up(); break; }
-                mbar_arrive_expect_tx(&q_full[qs], 2 * KB_T);
-                tma_load_3d(sm + SM::Q + qs * 2 * KB_T, &tq, &q_full[qs], 0, c * C, unit);
-                tma_load_3d(sm + SM::Q + qs * 2 * KB_T + KB_T, &tq, &q_full[qs], 64, c * C, unit);
+                load_tile(sm + SM::Q + qs * 2 * KB_T, KB_T, &tq, &q_full[qs], c, unit);
                 ++q_issued[qs];
                 LZ_TRACE(pc, 16);
                 if (r >= NR && !bwait(&v_empty[s], r / NR - 1, abort_f)) { give_up(); break; }
-                mbar_arrive_expect_tx(&v_full[s], 2 * KB_T);
-                tma_load_3d(base + SLOT_V, &tv, &v_full[s], 0, c * C, kvu);
-                tma_load_3d(base + SLOT_V + KB_T, &tv, &v_full[s], 64, c * C, kvu);
+                load_tile(base + SLOT_V, KB_T, &tv, &v_full[s], c, kvu);
                 ++v_issued[s];
                 LZ_TRACE(pc, 17);
             }
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (cj < c_lo) continue;
                     const uint32_t kb = sb + SM::KV + ((cj - c_lo) % NR) * SLOT;
                     mma_chain(tmem + T_SC + 64 * j, smem_desc(qb, 16, 1024), smem_desc(kb, 16, 1024),
-                              j == NP ? id_sc_cur : id_sc_prev, 0u, 8, 32, 32, KB_T, KB_K);
+                              j == NP ? id_sc_cur : id_sc_prev, 0u, nk, 32, 32, KB_T, KB_K);
                 }
                 mma_commit(sc_full);
                 mma_commit(&q_empty[qs]);
@@ -573,7 +581,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 if (!unsafe_f[b]) {
                     const uint32_t ob = sb + SM::OP + b * OPB;
-                    mma_chain(tmem + TM::A, smem_desc(ob, 16, 1024), smem_desc(ob + 2 * KB_T, 16, 1024), id_a, 0u, 8,
+                    mma_chain(tmem + TM::A, smem_desc(ob, 16, 1024), smem_desc(ob + 2 * KB_T, 16, 1024), id_a, 0u, nk,
                               32, 32, KB_T, KB_T);
                     mma_commit(a_full);
                 } else {
@@ -613,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 {
                     const uint64_t dq = smem_desc(ob, 16, 1024);
 #pragma unroll 1
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < nk; ++kk)
                         mma_bf16_ts(tmem + T_Y, tmem + T_S16 + kk * 8, dq + ((((kk >> 2) * KB_T) + (kk & 3) * 32) >> 4),
                                     id_y1, kk > 0);
                 }
@@ -649,17 +657,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;
         const int j = 32 * quarter + lane;  // value dim = tensor-memory lane
         const uint32_t tl = tmem + tlane(quarter);
+        const bool live = j < d;            // lanes past d_v hold the zero padding: no stores
         {
             // Initial state: the state after the earlier segments, or S0
-            // (zero when not given) for the first segment.
-            const float *Si = seg > 0 ? (a.S_init ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * D * D + j
-                                                  : nullptr)
-                                      : (a.S0 ? a.S0 + (size_t)unit * D * D + j : nullptr);
+            // (zero when not given) for the first segment; zero padding.
+            const float *Si = !live ? nullptr
+                              : seg > 0 ? (a.S_init ? a.S_init + ((size_t)unit * (nseg - 1) + seg - 1) * d * d + j
+                                                    : nullptr)
+                                        : (a.S0 ? a.S0 + (size_t)unit * d * d + j : nullptr);
 #pragma unroll 1
             for (int cc = 0; cc < D; cc += 16) {
                 uint32_t z[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) z[e] = Si ? __float_as_uint(Si[(size_t)(cc + e) * D]) : 0u;
+                for (int e = 0; e < 16; ++e) z[e] = Si && cc + e < d ? __float_as_uint(Si[(size_t)(cc + e) * d]) : 0u;
                 tmem_st16(tl + T_S + cc, z);
             }
             tmem_wait_st();
@@ -672,7 +682,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             LZ_TRACE(py, 10);
             tc_fence_after();
             const int c0 = (c_begin + py) * C, n = min(C, L - c0);
-            __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * D + j;
+            __nv_bfloat16 *yp = a.y + ((size_t)unit * L + c0) * d + j;
             uint32_t r[4][16];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tl + T_Y + 16 * q4, r[q4]);
@@ -685,7 +695,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // two adjacent value dims of one token (4-byte stores): the even
             // lane token t, the odd lane token t + 1.
             const bool odd = lane & 1;
-            __nv_bfloat16 *yq = yp - (odd ? 1 : 0) + (odd ? D : 0);
+            __nv_bfloat16 *yq = yp - (odd ? 1 : 0) + (odd ? d : 0);
             const int t_odd = odd ? 1 : 0;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
@@ -695,8 +705,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
                     // even: (mine.lo, other.lo); odd: (other.hi, mine.hi)
                     const uint32_t out = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
-                    if (16 * q4 + e + t_odd < n)
-                        *reinterpret_cast<uint32_t *>(yq + (size_t)(16 * q4 + e) * D) = out;
+                    if (live && 16 * q4 + e + t_odd < n)
+                        *reinterpret_cast<uint32_t *>(yq + (size_t)(16 * q4 + e) * d) = out;
                 }
             LZ_TRACE(py, 11);
             return true;
@@ -714,7 +724,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // an unsafe chunk, so one product serves both.
             const bool one = !unsafe_f[b];
 #pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
+            for (int cb = 0; cb < d; cb += 32) {
                 uint32_t r0[16], r1[16];
                 tmem_ld16(tl + T_S + cb, r0);
                 tmem_ld16(tl + T_S + cb + 16, r1);
@@ -769,15 +779,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                           [&] { return nch == 0 || bwait(st_done, nch - 1, abort_f); })) {
                 tc_fence_after();
                 const float *Fv = vec + ((nch - 1) & 1) * NVEC * 128 + 256;
-                float *So = a.S_out + (size_t)unit * D * D + j;
+                float *So = a.S_out + (size_t)unit * d * d + j;
 #pragma unroll 1
-                for (int cc = 0; cc < D; cc += 16) {
+                for (int cc = 0; cc < d; cc += 16) {
                     uint32_t r[16];
                     tmem_ld16(tl + T_S + cc, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        So[(size_t)(cc + e) * D] = nch == 0 ? __uint_as_float(r[e]) : __uint_as_float(r[e]) * Fv[cc + e];
+                        if (live)
+                            So[(size_t)(cc + e) * d] =
+                                nch == 0 ? __uint_as_float(r[e]) : __uint_as_float(r[e]) * Fv[cc + e];
                 }
             } else {
                 give_up();
@@ -792,14 +804,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int tp = tid - W_PREP * 32;
         const int p = tp & 63, hq = tp >> 6;       // key dims 2p, 2p+1; tokens 16 hq .. 16 hq + 15
         const uint32_t kblk = (p / 32), kbyte = (p % 32) * 4;
-        // Gate logits of the chunk being prepared, loaded one chunk ahead.
-        const __nv_bfloat16 *gsrc = a.g + (size_t)unit * L * D + 2 * p;
+        // Gate logits of the chunk being prepared, loaded one chunk ahead
+        // (+inf, no decay, past the end and in the padding dims).
+        const bool live = 2 * p < d;        // warp-uniform
+        const __nv_bfloat16 *gsrc = a.g + (size_t)unit * L * d + 2 * p;
         uint32_t gr[16];
         auto load_g = [&](int c) {
             const int t0 = c * C + 16 * hq;
 #pragma unroll
             for (int tt = 0; tt < 16; ++tt)
-                gr[tt] = t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
+                gr[tt] = live && t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * d) : 0x7F807F80u;
         };
         if (c_begin < c_end) load_g(c_begin);
         float2 Fp = make_float2(1.f, 1.f);         // F of the previous chunk (1: Shat = S at the start)
@@ -850,6 +864,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // QR = q / Z; every factor lies in [2^-SPAN2_MAX, 2^SPAN2_MAX].
                 const float2 er = make_float2(rcp(h0.x), rcp(h0.y));     // 2^r
                 float2 R = hq == 0 ? er : hq == 1 ? mul2(er, T[0]) : hq == 2 ? make_float2(1.f, 1.f) : T[2];
+                if (live)
 #pragma unroll
                 for (int tt = 0; tt < 16; ++tt) {
                     R = mul2(R, iv[tt]);
@@ -887,7 +902,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
                     for (int tt = 0; tt < 16; ++tt) {
                         const uint32_t gv =
-                            t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * D) : 0x7F807F80u;
+                            live && t0 + tt < L ? ld_stream_u32(gsrc + (size_t)(t0 + tt) * d) : 0x7F807F80u;
                         run = add2(run, log2_sigmoid2(bf2_to_f2(gv)));
                         *reinterpret_cast<float2 *>(bz + (16 * hq + tt) * D + 2 * p) = run;
                     }
@@ -915,7 +930,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     float acc[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-                    for (int i = 0; i < D; ++i) {
+                    for (int i = 0; i < d; ++i) {
                         const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                             qrow + (i / 64) * KB_T + sw128_offset(t, (i % 64) * 2)));
                         const float bt = bz[t * D + i];
@@ -970,15 +985,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         // prompt advanced pos at its start).
         if (!failed && a.S_out && last_seg) {
             const int first = max(0, L - w);
-            const __nv_bfloat16 *kp = a.k + (size_t)kvu * L * D, *vp = a.v + (size_t)kvu * L * D;
-            __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * D, *rv = a.ring_v + (size_t)unit * w * D;
-            for (int e = tp; e < (L - first) * (D / 8); e += PREP_N) {
-                const int tau = first + e / (D / 8), i8 = (e % (D / 8)) * 8;
+            const __nv_bfloat16 *kp = a.k + (size_t)kvu * L * d, *vp = a.v + (size_t)kvu * L * d;
+            __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * d, *rv = a.ring_v + (size_t)unit * w * d;
+            for (int e = tp; e < (L - first) * (d / 8); e += PREP_N) {
+                const int tau = first + e / (d / 8), i8 = (e % (d / 8)) * 8;
                 const size_t slot = (size_t)((p0 + tau) % w);
-                *reinterpret_cast<uint4 *>(rk + slot * D + i8) =
-                    *reinterpret_cast<const uint4 *>(kp + (size_t)tau * D + i8);
-                *reinterpret_cast<uint4 *>(rv + slot * D + i8) =
-                    *reinterpret_cast<const uint4 *>(vp + (size_t)tau * D + i8);
+                *reinterpret_cast<uint4 *>(rk + slot * d + i8) =
+                    *reinterpret_cast<const uint4 *>(kp + (size_t)tau * d + i8);
+                *reinterpret_cast<uint4 *>(rv + slot * d + i8) =
+                    *reinterpret_cast<const uint4 *>(vp + (size_t)tau * d + i8);
             }
             if (!a.cont && h == 0 && tp == 0) a.pos[unit / a.H] = L;
         }

@@ -73,6 +73,9 @@ WORKLOADS = {
     "decode": Workload("decode", 64, 32, 64, 128, 128, 64, 4, 1.0, BF16, 3.0, 1.0, 3, decode_steps=1024),
     "long_context": Workload("long_context", 1, 32, 65536, 128, 128, 64, 4, 1.0, BF16, 4.0, 1.0, 4,
                              decode_steps=128),
+    # head dim 64 (a Llama-3.2-1B-shaped layer: 32 heads of 64), otherwise
+    # the headline prefill's recipe
+    "d64": Workload("d64", 4, 32, 4096, 64, 64, 64, 4, 1.0, BF16, 3.0, 1.0, 5),
 }
 
 

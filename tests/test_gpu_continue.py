@@ -70,7 +70,7 @@ def _run_pieces(inp, w, pieces, first_is_prefill=True):
 
 CASES = [
     # name, dtype, B, H, pieces, d, w, m, g_mean, g_std, alpha
-    # warp-specialised tensor-core path (bf16, d = 128, w <= 65)
+    # warp-specialised tensor-core path (bf16, d = 128 or 64, w <= 65)
     ("ws_two_pieces", "bf16", 2, 2, (200, 150), 128, 64, 4, 3.0, 1.0, 1.0),
     ("ws_short_history", "bf16", 1, 3, (10, 130), 128, 64, 4, 3.0, 1.0, 1.0),
     ("ws_short_continuation", "bf16", 1, 2, (300, 20), 128, 64, 4, 3.0, 1.0, 0.7),
@@ -82,11 +82,15 @@ CASES = [
     ("ws_segments", "bf16", 1, 2, (500, 3000), 128, 64, 4, 3.0, 1.0, 1.0),
     ("ws_segments_short_history", "bf16", 1, 1, (5, 2100), 128, 48, 4, 0.0, 2.0, 0.5),
     ("ws_segments_window_one", "bf16", 1, 2, (300, 1500), 128, 1, 2, 3.0, 1.0, 1.0),
+    ("ws_d64_two_pieces", "bf16", 2, 2, (200, 150), 64, 64, 4, 3.0, 1.0, 1.0),
+    ("ws_d64_short_history", "bf16", 1, 3, (10, 130, 70), 64, 48, 4, 3.0, 1.0, 1.0),
+    ("ws_d64_strong_decay", "bf16", 1, 2, (300, 260), 64, 64, 4, -8.0, 4.0, 1.0),
+    ("ws_d64_window_65", "bf16", 1, 2, (70, 140), 64, 65, 4, 3.0, 1.0, 1.0),
     # tensor-core path with a two-chunk window band (bf16, d = 128, w > 65)
     ("tc_window_100", "bf16", 1, 2, (300, 200), 128, 100, 4, 3.0, 1.0, 1.0),
     ("tc_window_128_short_history", "bf16", 1, 2, (30, 200, 70), 128, 128, 16, 3.0, 1.0, 1.0),
     ("tc_strong_decay", "bf16", 1, 2, (129, 300), 128, 80, 4, -8.0, 4.0, 0.5),
-    # CUDA-core path (fp32, or d = 64)
+    # CUDA-core path (fp32, or bf16 d = 64 with w > 65)
     ("simt_f32_d128", "f32", 1, 2, (150, 130), 128, 64, 4, 3.0, 1.0, 1.0),
     ("simt_f32_d64", "f32", 2, 2, (37, 100, 64), 64, 16, 4, 3.0, 1.0, 0.5),
     ("simt_bf16_d64_w100", "bf16", 1, 2, (90, 160), 64, 100, 4, 3.0, 1.0, 1.0),
@@ -108,7 +112,7 @@ def test_pieces_match_one_pass(case):
     _check_state(st, inp, Ltot, S_ref, tol)
 
 
-@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 100), ("f32", 64, 16)])
+@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 100), ("bf16", 64, 64), ("f32", 64, 16)])
 def test_continue_from_empty_state_is_a_prefill(dt, d, w):
     inp = _inputs(f"empty_{dt}_{d}_{w}", dt, 2, 2, 230, d, w, 4)
     y_gpu, st = _run_pieces(inp, w, (230,), first_is_prefill=False)
@@ -131,7 +135,7 @@ def test_empty_continuation_leaves_the_state():
     assert torch.equal(S, st.S) and torch.equal(rk, st.ring_k) and torch.equal(pos, st.pos)
 
 
-@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 128), ("f32", 128, 40)])
+@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 128), ("bf16", 64, 64), ("f32", 128, 40)])
 def test_sequences_at_different_positions(dt, d, w):
     """One call continues sequences that have consumed 0, 5 and 300 tokens:
     the state is written by hand from the oracle (S, ring slots p % w, pos)."""

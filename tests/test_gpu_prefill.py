@@ -74,6 +74,19 @@ CASES = [
     ("segments_w100", "bf16", 1, 2, 2000, 128, 100, 4, 3.0, 1.0, 1.0),
     ("segments_w128_strong_decay", "bf16", 1, 2, 2100, 128, 128, 8, 0.0, 2.0, 0.5),
     ("segments_w66_exact_intra", "bf16", 1, 1, 1500, 128, 66, 2, -8.0, 4.0, 1.0),
+    # head dim 64 on the tensor-core pipeline (tiles zero-padded to 128)
+    ("d64_window_one", "bf16", 1, 2, 150, 64, 1, 3, 3.0, 1.0, 1.0),
+    ("d64_window_65", "bf16", 1, 2, 333, 64, 65, 4, 3.0, 1.0, 1.0),
+    ("d64_extreme_decay_exact_intra", "bf16", 1, 2, 300, 64, 64, 4, -8.0, 4.0, 1.0),
+    ("d64_mixed_decay", "bf16", 1, 3, 520, 64, 32, 4, -1.0, 3.0, 0.8),
+    ("d64_open_gates_no_meta", "bf16", 1, 2, 200, 64, 48, 0, 12.0, 0.5, 1.0),
+    ("d64_max_meta", "bf16", 1, 2, 300, 64, 64, 16, 3.0, 1.0, 1.0),
+    ("d64_single_token", "bf16", 2, 2, 1, 64, 16, 4, 3.0, 1.0, 0.5),
+    ("d64_L_below_w", "bf16", 2, 2, 40, 64, 64, 4, 3.0, 1.0, 1.0),
+    ("d64_alpha_zero", "bf16", 1, 2, 190, 64, 64, 4, 3.0, 1.0, 0.0),
+    ("d64_long_prompt_few_units", "bf16", 1, 2, 3000, 64, 64, 4, 3.0, 1.0, 0.7),
+    ("d64_more_units_than_sms", "bf16", 5, 32, 70, 64, 64, 4, 3.0, 1.0, 1.0),
+    ("d64_w100_cuda_cores", "bf16", 1, 2, 300, 64, 100, 4, 3.0, 1.0, 1.0),
 ]
 
 
@@ -115,6 +128,12 @@ def _full_size(wl_name):
 def test_llama3_8b_full_size_all_units():
     """B4 H32 L4096 d128 bf16 in one launch; all 128 units against the oracle."""
     _full_size("llama3_8b")
+
+
+def test_d64_full_size_all_units():
+    """B4 H32 L4096 d64 bf16 (the tensor-core pipeline on zero-padded
+    tiles) in one launch; all 128 units against the oracle."""
+    _full_size("d64")
 
 
 def test_decay_stress_full_size_all_units():

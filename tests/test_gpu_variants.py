@@ -70,7 +70,9 @@ CASES = [
     ("ws_segments_gqa", "bf16", 1, 4, 2, 1600, 128, 64, 4),
     ("tc_gqa2", "bf16", 1, 4, 2, 260, 128, 100, 4),
     ("simt_f32_gqa2", "f32", 1, 4, 2, 150, 64, 16, 4),
-    ("simt_bf16_d64_mqa", "bf16", 2, 2, 1, 130, 64, 32, 3),
+    ("ws_d64_mqa", "bf16", 2, 2, 1, 130, 64, 32, 3),
+    ("ws_d64_gqa2", "bf16", 2, 4, 2, 200, 64, 64, 4),
+    ("simt_bf16_d64_w100_gqa2", "bf16", 1, 4, 2, 160, 64, 100, 4),
     ("ws_per_head_alpha_only", "bf16", 1, 3, 3, 140, 128, 64, 4),
 ]
 
@@ -92,7 +94,7 @@ def test_prefill_variants(case):
         assert torch.equal(st.ring_k[:, :, p % w].cpu(), kx[:, :, p])
 
 
-@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 100), ("f32", 64, 16)])
+@pytest.mark.parametrize("dt,d,w", [("bf16", 128, 64), ("bf16", 128, 100), ("bf16", 64, 64), ("f32", 64, 16)])
 def test_continue_and_decode_variants(dt, d, w):
     """prefill 90 + continue 60 + 3 decode steps, grouped heads, per-head alpha."""
     Bn, H, Hkv, steps = 2, 4, 2, 3
