@@ -24,6 +24,8 @@
 // States and state gradients are kept in bf16, row = key dim.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "prefill_ws.cuh"
 #include "sm100.cuh"
@@ -352,6 +354,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     float *rv = reinterpret_cast<float *>(sm + QO_VEC), *tot = rv + 128, *dC = tot + 512;
     int *flags = reinterpret_cast<int *>(dC + 64 * 16);
     float *bq = reinterpret_cast<float *>(sm + QO_B);
+    // Element (t, i) of bq sits at column i ^ (t mod 32) of row t: a warp
+    // reading one column of 16 rows (two column halves) hits 32 banks.
+    auto bx = [](int t, int i) { return t * D + (i ^ (t & 31)); };
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + QO_BAR);
     uint64_t *bar_in = bars, *bar_s = bars + 1, *bar_mma = bars + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + QO_TSLOT);
@@ -432,8 +437,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int t = 16 * hq + tt;
                 const float2 bt = pf.b[tt];
                 wide |= fabsf(bt.x - r2.x) > SPAN2_MAX || fabsf(bt.y - r2.y) > SPAN2_MAX;
-                bq[t * D + 2 * p] = bt.x;
-                bq[t * D + 2 * p + 1] = bt.y;
+                bq[bx(t, 2 * p)] = bt.x;
+                bq[bx(t, 2 * p + 1)] = bt.y;
                 const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(
                     sm + QO_KC + (p / 32) * KB_K + sw128_offset(t, kbyte)));
                 *reinterpret_cast<uint32_t *>(sm + QO_KR + kblk + sw128_offset(t, kbyte)) =
@@ -721,7 +726,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int i = i0 + e;
-                    const float bt = bq[t * D + i];
+                    const float bt = bq[bx(t, i)];
                     const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                         sm + QO_Q + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
                     const float inter = ex2(bt) * __uint_as_float(g1[e]);
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const int i = i0 + e;
                             const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                                 sm + QO_KC + (i / 64) * KB_K + sw128_offset(s2, (i % 64) * 2)));
-                            intra[e] += dA * kv * ex2(bq[t * D + i] - bq[s2 * D + i]);
+                            intra[e] += dA * kv * ex2(bq[bx(t, i)] - bq[bx(s2, i)]);
                         }
                     }
 #pragma unroll
@@ -834,6 +839,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     float *rv = reinterpret_cast<float *>(sm + KO_VEC), *blv = rv + 128, *tot = blv + 128, *Ep = tot + 512;
     float *bk = reinterpret_cast<float *>(sm + KO_B);  // phase B: b [64][128]
     float *yo = reinterpret_cast<float *>(sm + KO_QN);  // after the gate products: k * dk_inter [64][128]
+    // Element (t, i) of bk / yo sits at column i ^ (t mod 32) of row t, so
+    // that a warp reading one column of 16 rows (two column halves) hits 32
+    // distinct banks; a row read along i stays a permutation of one row.
+    auto bx = [](int t, int i) { return t * D + (i ^ (t & 31)); };
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + KO_BAR);
     uint64_t *bar_in = bars, *bar_mma = bars + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + KO_TSLOT);
@@ -1039,8 +1048,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int t2 = 16 * hq + tt;
                 const float2 bt = pf.b[tt];
                 wide |= fabsf(bt.x - r2.x) > SPAN2_MAX || fabsf(bt.y - r2.y) > SPAN2_MAX;
-                bk[t2 * D + 2 * p] = bt.x;
-                bk[t2 * D + 2 * p + 1] = bt.y;
+                bk[bx(t2, 2 * p)] = bt.x;
+                bk[bx(t2, 2 * p + 1)] = bt.y;
                 const uint32_t o = kblk + sw128_offset(t2, kbyte);
                 const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + KO_Q + o));
                 const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + KO_K + o));
@@ -1072,41 +1081,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         // ---- E1b: tril(A) (exact on the CUDA cores for a wide chunk); KL = k 2^{b_last - b}
         {
-            uint32_t r[2][16];
             if (warp < 4) {
+                uint32_t r[2][16];
                 tmem_ld16_x2<16>(tl + KT_A, r[0]);
                 tmem_ld16_x2<16>(tl + KT_A + 32, r[1]);
                 tmem_wait_ld();
+                if (!unsafe) {
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int s0 = 32 * jj + 16 * hs;
-                    uint32_t pk[8];
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int s0 = 32 * jj + 16 * hs;
+                        uint32_t pk[8];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        float va[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int s2 = s0 + e + u;
-                            float av = __uint_as_float(r[jj][e + u]);
-                            if (unsafe && t < n && s2 <= t) {
-                                av = 0.f;
-                                for (int i = 0; i < D; ++i) {
-                                    const uint32_t ob = (i / 64) * TILE;
-                                    const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                        sm + KO_Q + ob + sw128_offset(t, (i % 64) * 2)));
-                                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                        sm + KO_K + ob + sw128_offset(s2, (i % 64) * 2)));
-                                    av += qv * kv * ex2(bk[t * D + i] - bk[s2 * D + i]);
-                                }
-                            }
-                            va[u] = (t < n && s2 <= t) ? av : 0.f;
-                        }
-                        pk[e / 2] = f2_to_bf2(va[0], va[1]);
+                        for (int e = 0; e < 16; e += 2)
+                            pk[e / 2] = f2_to_bf2(t < n && s0 + e <= t ? __uint_as_float(r[jj][e]) : 0.f,
+                                                  t < n && s0 + e + 1 <= t ? __uint_as_float(r[jj][e + 1]) : 0.f);
+                        *reinterpret_cast<uint4 *>(sm + KO_AT + sw128_offset(t, s0 * 2)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(sm + KO_AT + sw128_offset(t, s0 * 2 + 16)) =
+                            make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
-                    *reinterpret_cast<uint4 *>(sm + KO_AT + sw128_offset(t, s0 * 2)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(sm + KO_AT + sw128_offset(t, s0 * 2 + 16)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                } else {
+                    // exact, one score at a time (a rare path: small code)
+#pragma unroll 1
+                    for (int sx = 0; sx < 32; ++sx) {
+                        const int s2 = 32 * (sx / 16) + 16 * hs + sx % 16;
+                        float av = 0.f;
+                        if (t < n && s2 <= t) {
+#pragma unroll 1
+                            for (int i = 0; i < D; ++i) {
+                                const uint32_t ob = (i / 64) * TILE;
+                                const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                    sm + KO_Q + ob + sw128_offset(t, (i % 64) * 2)));
+                                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                    sm + KO_K + ob + sw128_offset(s2, (i % 64) * 2)));
+                                av += qv * kv * ex2(bk[bx(t, i)] - bk[bx(s2, i)]);
+                            }
+                        }
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + KO_AT + sw128_offset(t, s2 * 2)) = __float2bfloat16_rn(av);
+                    }
                 }
             }
             {
@@ -1115,9 +1127,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int s2 = e / 64, ip = e % 64, i = 2 * ip;
                     const uint32_t o = (i / 64) * TILE + sw128_offset(s2, (i % 64) * 2);
                     const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + KO_K + o));
-                    const float bl0 = bk[(C - 1) * D + i], bl1 = bk[(C - 1) * D + i + 1];
+                    const float bl0 = bk[bx(C - 1, i)], bl1 = bk[bx(C - 1, i + 1)];
                     *reinterpret_cast<uint32_t *>(sm + KO_DYN + o) =
-                        f2_to_bf2(kv.x * ex2(bl0 - bk[s2 * D + i]), kv.y * ex2(bl1 - bk[s2 * D + i + 1]));
+                        f2_to_bf2(kv.x * ex2(bl0 - bk[bx(s2, i)]), kv.y * ex2(bl1 - bk[bx(s2, i + 1)]));
                 }
             }
         }
@@ -1185,38 +1197,47 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_wait_ld();
                 uint32_t dkp[8], dvp[8];
                 float dkv[16];
+                // The exact intra-chunk part of a wide chunk is a separate
+                // copy of the loop, so that the common one holds no rare code.
+                auto elems = [&](auto wide) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i = i0 + e;
-                    dkv[e] = 0.f;
-                    if (rowok) {
-                        const float bs = bk[t * D + i];
-                        const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                            sm + KO_K + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
-                        const float inter = ex2(blv[i] - bs) * __uint_as_float(g1[e]);
-                        float intra = 0.f, kintra = 0.f;
-                        if (!unsafe) {
-                            const float g2v = __uint_as_float(g2[e]);
-                            intra = ex2(rv[i] - bs) * g2v;
-                            kintra = __bfloat162float(__float2bfloat16_rn(kv * ex2(rv[i] - bs))) * g2v;
-                        } else {
-                            for (int t2 = t; t2 < n; ++t2) {
-                                const float dA = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                    sm + KO_DAT + sw128_offset(t2, t * 2)));
-                                const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                    sm + KO_Q + (i / 64) * TILE + sw128_offset(t2, (i % 64) * 2)));
-                                intra += dA * qv * ex2(bk[t2 * D + i] - bs);
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = i0 + e;
+                        dkv[e] = 0.f;
+                        if (rowok) {
+                            const float bs = bk[bx(t, i)];
+                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                sm + KO_K + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
+                            const float inter = ex2(blv[i] - bs) * __uint_as_float(g1[e]);
+                            float intra = 0.f, kintra = 0.f;
+                            if constexpr (!decltype(wide)::value) {
+                                const float g2v = __uint_as_float(g2[e]);
+                                intra = ex2(rv[i] - bs) * g2v;
+                                kintra = __bfloat162float(__float2bfloat16_rn(kv * ex2(rv[i] - bs))) * g2v;
+                            } else {
+#pragma unroll 1
+                                for (int t2 = t; t2 < n; ++t2) {
+                                    const float dA = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                        sm + KO_DAT + sw128_offset(t2, t * 2)));
+                                    const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                        sm + KO_Q + (i / 64) * TILE + sw128_offset(t2, (i % 64) * 2)));
+                                    intra += dA * qv * ex2(bk[bx(t2, i)] - bs);
+                                }
+                                kintra = kv * intra;
                             }
-                            kintra = kv * intra;
+                            dkv[e] = inter + intra + __uint_as_float(ka[e]);
+                            term[jj][e] = xqv[e] - kintra;
+                            yo[bx(t, i)] = kv * inter;  // the QR / KL slot: read by M2b, which is done
+                        } else {
+                            term[jj][e] = 0.f;
+                            yo[bx(t, i)] = 0.f;
                         }
-                        dkv[e] = inter + intra + __uint_as_float(ka[e]);
-                        term[jj][e] = xqv[e] - kintra;
-                        yo[t * D + i] = kv * inter;  // the QR / KL slot: read by M2b, which is done
-                    } else {
-                        term[jj][e] = 0.f;
-                        yo[t * D + i] = 0.f;
                     }
-                }
+                };
+                if (!unsafe)
+                    elems(std::false_type{});
+                else
+                    elems(std::true_type{});
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
                     dkp[e / 2] = f2_to_bf2(dkv[e], dkv[e + 1]);
@@ -1235,7 +1256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) bk[t * D + 64 * colh + 32 * jj + 16 * hs + e] = term[jj][e];
+                for (int e = 0; e < 16; ++e) bk[bx(t, 64 * colh + 32 * jj + 16 * hs + e)] = term[jj][e];
         }
         // ---- dg = dlog gamma * sigmoid(-g).  sigmoid(-g) = 2^{log2 sigmoid(-g)}
         // for every element first (into the state-gradient slot: its readers
@@ -1255,8 +1276,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         {
             float sr = 0.f, sf = 0.f;
             for (int t2 = h0; t2 < h1; ++t2) {
-                sr += bk[t2 * D + i];
-                sf += yo[t2 * D + i];
+                sr += bk[bx(t2, i)];
+                sf += yo[bx(t2, i)];
             }
             __syncthreads();  // Ep (the E parts) is read below, before it is reused
             const float E = (Ep[i] + Ep[128 + i]) * ex2(blv[i]);
@@ -1267,13 +1288,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             float run = (half == 0 ? part[i] : 0.f) + E;  // reverse: later rows first
             float f = half == 1 ? part[128 + i] : 0.f;   // forward exclusive prefix
             for (int t2 = h0; t2 < h1; ++t2) {  // forward prefix of k dk_inter, in place
-                const float x = yo[t2 * D + i];
-                yo[t2 * D + i] = f;
+                const float x = yo[bx(t2, i)];
+                yo[bx(t2, i)] = f;
                 f += x;
             }
             for (int t2 = h1 - 1; t2 >= h0; --t2) {
-                run += bk[t2 * D + i];
-                a.dg[((size_t)unit * L + c0 + t2) * D + i] = __float2bfloat16_rn((run + yo[t2 * D + i]) * sg[t2 * D + i]);
+                run += bk[bx(t2, i)];
+                a.dg[((size_t)unit * L + c0 + t2) * D + i] = __float2bfloat16_rn((run + yo[bx(t2, i)]) * sg[t2 * D + i]);
             }
         }
     } while (false);
