@@ -510,6 +510,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
             lse2 = M2 + ws::lg2(sum);
             if (rowok && hs == 0) a.lse2[(size_t)unit * L + c0 + t] = lse2;
+            if (hs == 0) tot[t] = lse2;  // for warps 4-7 (tot is free after the prep)
             // P (bf16) for P V
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -580,11 +581,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             s_issued = 1;
         }
         tc_fence_after();
-        // ---- E2: D_t = alpha dy . ya, d alpha; score gradients; d mu
-        if (warp < 4) {
+        // ---- E2: D_t = alpha dy . ya, d alpha; score gradients; d mu.
+        // All eight warps: warp w takes rows 16 (w % 4) .. + 15 and the
+        // column groups jj = 2 (w / 4), 2 (w / 4) + 1 (32 columns each).
+        {
+            const int g = warp >> 2;
+            if (g == 1) lse2 = tot[t];
             float dot = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
+            for (int jx = 0; jx < 2; ++jx) {
+                const int jj = 2 * g + jx;
                 uint32_t r[16];
                 tmem_ld16_x2<16>(tl + QT_YA + 32 * jj, r);
                 tmem_wait_ld();
@@ -598,26 +604,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+            float *part = tot + 128;  // [2][64] row partials of the two column halves
+            if (hs == 0) part[64 * g + t] = dot;
+            __syncthreads();
+            dot = part[t] + part[64 + t];
             if (!rowok) dot = 0.f;
             const float Dt = alpha * dot;
-            if (rowok && hs == 0) a.drow[(size_t)unit * L + c0 + t] = Dt;
-            // d alpha: this warp's rows
-            float da = hs == 0 ? dot : 0.f;
+            if (g == 0) {
+                if (rowok && hs == 0) a.drow[(size_t)unit * L + c0 + t] = Dt;
+                // d alpha: this warp's rows
+                float da = hs == 0 ? dot : 0.f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-            if (lane == 0) atomicAdd(a.dalpha + (a.alpha_h ? h : 0), da);
-            // dSC = P (alpha dP - D_t) over the band, dC = P_meta (0 - D_t)
-            uint32_t r[4][16], rd[4][16], rm[16];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                tmem_ld16_x2<16>(tl + QT_SC + 32 * jj, r[jj]);
-                tmem_ld16_x2<16>(tl + QT_DP + 32 * jj, rd[jj]);
+                for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+                if (lane == 0) atomicAdd(a.dalpha + (a.alpha_h ? h : 0), da);
             }
-            tmem_ld16(tl + QT_SC + 128, rm);
+            // dSC = P (alpha dP - D_t) over the band, dC = P_meta (0 - D_t)
+            uint32_t r[2][16], rd[2][16];
+#pragma unroll
+            for (int jx = 0; jx < 2; ++jx) {
+                tmem_ld16_x2<16>(tl + QT_SC + 32 * (2 * g + jx), r[jx]);
+                tmem_ld16_x2<16>(tl + QT_DP + 32 * (2 * g + jx), rd[jx]);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int col0 = 32 * jj + 16 * hs;
+            for (int jx = 0; jx < 2; ++jx) {
+                const int col0 = 32 * (2 * g + jx) + 16 * hs;
                 uint32_t pk[8];
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
@@ -626,8 +637,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int u = 0; u < 2; ++u) {
                         const int col = col0 + e + u;
                         const bool valid = rowok && col >= lo && col <= hi;
-                        const float pr = ex2(fmaf(__uint_as_float(r[jj][e + u]), LOG2E, -lse2));
-                        dv2[u] = valid ? pr * (alpha * __uint_as_float(rd[jj][e + u]) - Dt) : 0.f;
+                        const float pr = ex2(fmaf(__uint_as_float(r[jx][e + u]), LOG2E, -lse2));
+                        dv2[u] = valid ? pr * (alpha * __uint_as_float(rd[jx][e + u]) - Dt) : 0.f;
                     }
                     pk[e / 2] = f2_to_bf2(dv2[0], dv2[1]);
                 }
@@ -637,24 +648,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *reinterpret_cast<uint4 *>(sm + o + sw128_offset(t, (col0 % 64) * 2 + 16)) =
                     make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-            if (hs == 0) {
-                uint32_t pk[8];
+            if (g == 1) {
+                uint32_t rm[16];
+                tmem_ld16(tl + QT_SC + 128, rm);
+                tmem_wait_ld();
+                if (hs == 0) {
+                    uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float dv2[2];
+                    for (int e = 0; e < 16; e += 2) {
+                        float dv2[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int j = e + u;
-                        const float pr = ex2(fmaf(__uint_as_float(rm[j]), LOG2E, -lse2));
-                        dv2[u] = (rowok && j < m) ? pr * (0.f - Dt) : 0.f;
-                        dC[t * 16 + j] = dv2[u];
+                        for (int u = 0; u < 2; ++u) {
+                            const int j = e + u;
+                            const float pr = ex2(fmaf(__uint_as_float(rm[j]), LOG2E, -lse2));
+                            dv2[u] = (rowok && j < m) ? pr * (0.f - Dt) : 0.f;
+                            dC[t * 16 + j] = dv2[u];
+                        }
+                        pk[e / 2] = f2_to_bf2(dv2[0], dv2[1]);
                     }
-                    pk[e / 2] = f2_to_bf2(dv2[0], dv2[1]);
+                    *reinterpret_cast<uint4 *>(sm + QO_DSC + 2 * TILE + sw128_offset(t, 0)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(sm + QO_DSC + 2 * TILE + sw128_offset(t, 16)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
-                *reinterpret_cast<uint4 *>(sm + QO_DSC + 2 * TILE + sw128_offset(t, 0)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(sm + QO_DSC + 2 * TILE + sw128_offset(t, 16)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
         }
         fence_proxy_async_smem();
@@ -662,12 +678,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         // d mu[h][j][i] += sum_t dC[t][j] q[t][i]
         for (int e = tid; e < m * D; e += THREADS) {
             const int j = e / D, i = e % D;
-            float acc = 0.f;
-            for (int tt = 0; tt < n; ++tt)
-                acc += dC[tt * 16 + j] *
-                       __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                           sm + QO_Q + (i / 64) * TILE + sw128_offset(tt, (i % 64) * 2)));
-            atomicAdd(&a.dmu[((size_t)h * m + j) * D + i], acc);
+            const uint8_t *qcol = sm + QO_Q + (i / 64) * TILE;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums over the tokens
+            for (int t0 = 0; t0 < n; t0 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int tt = t0 + u;
+                    if (tt < n)
+                        acc[u] += dC[tt * 16 + j] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                                        qcol + sw128_offset(tt, (i % 64) * 2)));
+                }
+            }
+            atomicAdd(&a.dmu[((size_t)h * m + j) * D + i], (acc[0] + acc[1]) + (acc[2] + acc[3]));
         }
         if (!cta_wait(bar_s, 0)) break;
         tc_fence_after();
@@ -907,6 +929,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool qrow_ok = nxt ? t < nn : t < n;
     const float l2 = qrow_ok ? a.lse2[(size_t)unit * L + tq_row] : 0.f;
     const float Dt = qrow_ok ? a.drow[(size_t)unit * L + tq_row] : 0.f;
+    // The state before this chunk, row i = tid % 128, columns 64 (tid / 128)
+    // .. + 63, fetched while the tiles load (for the later chunks' share of
+    // dlog gamma below).
+    uint4 sv[8];
+    {
+        const uint4 *Sp = reinterpret_cast<const uint4 *>(a.Sb + ((size_t)unit * nch + c) * D * D +
+                                                          (size_t)(tid & 127) * D + 64 * (tid >> 7));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sv[u] = Sp[u];
+    }
     int unsafe = 0;
     do {
         if (!cta_wait(bar_in, 0)) break;
@@ -930,11 +962,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         // (scaled by 2^{b_last} later): row i, columns 64 half .. + 63
         {
             const int i = tid & 127, half = tid >> 7;
-            const uint4 *Sp = reinterpret_cast<const uint4 *>(a.Sb + ((size_t)unit * nch + c) * D * D + (size_t)i * D +
-                                                              64 * half);
-            uint4 sv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) sv[u] = Sp[u];
             float acc = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -1158,6 +1185,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             commit();
         }
+        // q * dq_gate of this thread's row and columns, fetched while the
+        // gate products run
+        float4 xq4[2][4];
+        if (t < n) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const float4 *xp = reinterpret_cast<const float4 *>(
+                    a.xq + ((size_t)unit * L + c0 + t) * D + 64 * (warp >> 2) + 32 * jj + 16 * hs);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) xq4[jj][u] = xp[u];
+            }
+        }
         if (!mma_wait()) break;
         tc_fence_after();
         // ---- E2: dk, dv; the dlog gamma terms.  With dk_gate = dk_inter +
@@ -1180,10 +1219,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t g1[16], g2[16], ka[16], vv[16];
                 float xqv[16];
                 if (rowok) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(a.xq + row * D + i0);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float4 x4 = xp[u];
+                        const float4 x4 = xq4[jj][u];
                         xqv[4 * u] = x4.x;
                         xqv[4 * u + 1] = x4.y;
                         xqv[4 * u + 2] = x4.z;
@@ -1200,21 +1238,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // The exact intra-chunk part of a wide chunk is a separate
                 // copy of the loop, so that the common one holds no rare code.
                 auto elems = [&](auto wide) {
+                    // shared-memory reads first, writes last: nothing in
+                    // between waits on an aliasing store
+                    float bsv[16], kvv[16], yov[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int i = i0 + e;
-                        dkv[e] = 0.f;
-                        if (rowok) {
-                            const float bs = bk[bx(t, i)];
-                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                sm + KO_K + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
-                            const float inter = ex2(blv[i] - bs) * __uint_as_float(g1[e]);
-                            float intra = 0.f, kintra = 0.f;
-                            if constexpr (!decltype(wide)::value) {
-                                const float g2v = __uint_as_float(g2[e]);
-                                intra = ex2(rv[i] - bs) * g2v;
-                                kintra = __bfloat162float(__float2bfloat16_rn(kv * ex2(rv[i] - bs))) * g2v;
-                            } else {
+                        bsv[e] = rowok ? bk[bx(t, i)] : 0.f;
+                        kvv[e] = rowok ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                             sm + KO_K + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)))
+                                       : 0.f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = i0 + e;
+                        const float bs = bsv[e], kv = kvv[e];
+                        const float inter = ex2(blv[i] - bs) * __uint_as_float(g1[e]);
+                        float intra = 0.f, kintra = 0.f;
+                        if constexpr (!decltype(wide)::value) {
+                            const float g2v = __uint_as_float(g2[e]);
+                            const float sc = ex2(rv[i] - bs);
+                            intra = sc * g2v;
+                            kintra = __bfloat162float(__float2bfloat16_rn(kv * sc)) * g2v;
+                        } else {
+                            if (rowok) {
 #pragma unroll 1
                                 for (int t2 = t; t2 < n; ++t2) {
                                     const float dA = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
@@ -1223,16 +1270,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         sm + KO_Q + (i / 64) * TILE + sw128_offset(t2, (i % 64) * 2)));
                                     intra += dA * qv * ex2(bk[bx(t2, i)] - bs);
                                 }
-                                kintra = kv * intra;
                             }
-                            dkv[e] = inter + intra + __uint_as_float(ka[e]);
-                            term[jj][e] = xqv[e] - kintra;
-                            yo[bx(t, i)] = kv * inter;  // the QR / KL slot: read by M2b, which is done
-                        } else {
-                            term[jj][e] = 0.f;
-                            yo[bx(t, i)] = 0.f;
+                            kintra = kv * intra;
                         }
+                        dkv[e] = rowok ? inter + intra + __uint_as_float(ka[e]) : 0.f;
+                        term[jj][e] = rowok ? xqv[e] - kintra : 0.f;
+                        yov[e] = rowok ? kv * inter : 0.f;
                     }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) yo[bx(t, i0 + e)] = yov[e];  // the QR / KL slot: M2b is done
                 };
                 if (!unsafe)
                     elems(std::false_type{});
