@@ -46,6 +46,7 @@ __global__ void state_init_kernel(float *S, size_t nS, uint4 *ring_k, uint4 *rin
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 // Stream-ordered scratch from a memory pool this library owns, one per
 // device.  Its release threshold is unlimited: memory a call frees stays
@@ -103,7 +104,9 @@ static lizard_status check_state(const lizard_state *st)
     if (!dtype_ok(st->dtype)) return LIZARD_ERR_INVALID_ARG;
     if (st->B < 0 || st->H < 1 || st->dk < 1 || st->dv < 1 || st->w < 1) return LIZARD_ERR_INVALID_ARG;
     if (!st->S || !st->ring_k || !st->ring_v || !st->pos) return LIZARD_ERR_INVALID_ARG;
-    if (!aligned16(st->S) || !aligned16(st->ring_k) || !aligned16(st->ring_v) || !aligned16(st->pos))
+    // pos is one int64 per sequence: 8-byte alignment, so that the state of
+    // a slice of the batch (pos + b0) is a valid state too
+    if (!aligned16(st->S) || !aligned16(st->ring_k) || !aligned16(st->ring_v) || !aligned8(st->pos))
         return LIZARD_ERR_INVALID_ARG;
     if (st->dk != st->dv || (st->dk != 64 && st->dk != 128)) return LIZARD_ERR_UNSUPPORTED;
     if (st->w > LIZARD_MAX_WINDOW) return LIZARD_ERR_UNSUPPORTED;

@@ -144,6 +144,17 @@ class LizardState:
         self.ring_v = torch.empty(B, H, w, dv, dtype=dtype, device=device)
         self.pos = torch.empty(B, dtype=torch.int64, device=device)
 
+    def batch(self, b0: int, b1: int) -> "LizardState":
+        """The state of sequences b0 .. b1-1: a view on the same buffers (the
+        batch is the outermost dim of every buffer), for calls on a slice of
+        the batch."""
+        if not 0 <= b0 < b1 <= self.B:
+            raise ValueError(f"batch slice {b0}:{b1} of {self.B}")
+        view = object.__new__(LizardState)
+        view.B, view.H, view.dk, view.dv, view.w, view.dtype = b1 - b0, self.H, self.dk, self.dv, self.w, self.dtype
+        view.S, view.ring_k, view.ring_v, view.pos = self.S[b0:b1], self.ring_k[b0:b1], self.ring_v[b0:b1], self.pos[b0:b1]
+        return view
+
     def c_struct(self) -> lizard_state:
         return lizard_state(self.S.data_ptr(), self.ring_k.data_ptr(), self.ring_v.data_ptr(),
                             self.pos.data_ptr(), self.B, self.H, self.dk, self.dv, self.w,

@@ -23,7 +23,8 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
  *     library never allocates, frees or retains them past the call.
  *   - Tensors are dense, row-major, head-major: [B][H][L][d] with the last
- *     dimension contiguous.  Every pointer must be 16-byte aligned.
+ *     dimension contiguous.  Every pointer must be 16-byte aligned (the
+ *     state's pos: 8-byte, see lizard_state).
  *   - Element type of q, k, v, g, meta keys, y and the ring buffer is the
  *     call's lizard_dtype (fp32 or bf16).  The recurrent state S is always
  *     fp32 and all accumulation is fp32.
@@ -84,7 +85,10 @@ typedef enum { LIZARD_F32 = 0, LIZARD_BF16 = 1 } lizard_dtype;
  *   ring_k  [B][H][w][dk]  dtype  keys of the last w tokens, token p in slot p % w
  *   ring_v  [B][H][w][dv]  dtype  values, same slots
  *   pos     [B] int64             tokens consumed so far by each sequence
- * All four are caller-owned device buffers.
+ * All four are caller-owned device buffers: S, ring_k and ring_v 16-byte
+ * aligned, pos 8-byte aligned.  The batch is the outermost dim of each, so
+ * sequences b0 .. b1-1 of a state form a state of their own (S + b0 H dk dv,
+ * ring_k + b0 H w dk, ring_v + b0 H w dv, pos + b0, B = b1 - b0).
  */
 typedef struct {
     float *S;

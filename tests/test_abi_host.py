@@ -124,7 +124,7 @@ def test_decode_rejects(lib, kw, code):
 
 def test_state_init_rejects(lib):
     assert lib.lizard_state_init(None, None) == INVALID
-    for bad in (state(S=None), state(pos=MIS), state(w=0), state(dtype=9)):
+    for bad in (state(S=None), state(pos=A + 4), state(w=0), state(dtype=9)):
         assert lib.lizard_state_init(ctypes.byref(bad), None) == INVALID
     assert lib.lizard_state_init(ctypes.byref(state(dk=80, dv=80)), None) == UNSUPPORTED
     assert lib.lizard_state_init(ctypes.byref(state(Bn=0)), None) == OK
@@ -241,7 +241,7 @@ def noalloc(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128, 
     (dict(v=MIS), INVALID), (dict(y=MIS), INVALID), (dict(dtype=7), INVALID), (dict(w=0), INVALID),
     (dict(m=-1), INVALID), (dict(L=-1), INVALID), (dict(H=0), INVALID), (dict(Bn=-1), INVALID),
     (dict(st=state(Bn=3)), INVALID), (dict(st=state(w=32)), INVALID), (dict(st=state(S=None)), INVALID),
-    (dict(st=state(pos=MIS)), INVALID), (dict(st=state(dtype=LA.LIZARD_F32)), INVALID),
+    (dict(st=state(pos=A + 4)), INVALID), (dict(st=state(dtype=LA.LIZARD_F32)), INVALID),
 ])
 def test_noalloc_rejects(lib, kw, code):
     assert noalloc(lib, **kw) == code
@@ -250,3 +250,26 @@ def test_noalloc_rejects(lib, kw, code):
 def test_noalloc_empty_calls_launch_nothing(lib):
     assert noalloc(lib, Bn=0) == OK
     assert noalloc(lib, q=None, k=None, v=None, g=None, y=None, L=0) == OK  # no state: nothing to reset
+
+
+def test_state_batch_view_shares_the_buffers():
+    """LizardState.batch(b0, b1) is a view of sequences b0 .. b1-1: the
+    struct it hands to the C ABI points into the parent's buffers."""
+    st = LA.LizardState(4, 2, 64, 64, 16, device="cpu")
+    v = st.batch(1, 3)
+    assert (v.B, v.H, v.dk, v.dv, v.w) == (2, 2, 64, 64, 16)
+    c = v.c_struct()
+    assert c.S == st.S[1].data_ptr() and c.pos == st.pos[1].data_ptr()
+    assert c.ring_k == st.ring_k[1].data_ptr() and c.ring_v == st.ring_v[1].data_ptr()
+    assert c.B == 2
+    with pytest.raises(ValueError):
+        st.batch(3, 3)
+    with pytest.raises(ValueError):
+        st.batch(2, 5)
+
+
+def test_state_pos_needs_only_8_byte_alignment(lib):
+    """pos of a batch slice (pos + b0) is only 8-byte aligned, and valid.
+    With B = 0 nothing is launched, so the fake addresses stay untouched."""
+    st = state(pos=A + 8, Bn=0)
+    assert lib.lizard_state_init(ctypes.byref(st), None) == LA.LIZARD_OK

@@ -5,6 +5,7 @@ import zlib
 import pytest
 import torch
 
+from hybrid_gated_linear_attn_b300 import LizardState, lizard_attn_prefill, lizard_check_device_status
 from hybrid_gated_linear_attn_b300.inputs import WORKLOADS, prefill_inputs, rel_l2
 from oracle import oracle as O
 from tests.gpu_helpers import TOL, ensure_built, gpu_prefill
@@ -140,3 +141,24 @@ def test_decay_stress_full_size_all_units():
     """B2 H32 L8192 d128 bf16, g ~ N(0, 2): cumulative decay far below fp32
     range; all 64 units against the oracle."""
     _full_size("decay_stress")
+
+
+def test_calls_on_batch_slices_with_state_views():
+    """One call per sequence, each on a LizardState.batch view, writes the
+    same outputs and state rows as the oracle run over the whole batch."""
+    wl = WORKLOADS["llama3_8b"].replace(B=3, H=2, L=700, seed=77)
+    inp = prefill_inputs(wl)
+    q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
+    st = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
+    y = torch.empty_like(v)
+    for b in range(wl.B):
+        lizard_attn_prefill(q[b:b + 1], k[b:b + 1], v[b:b + 1], g[b:b + 1], mu, wl.alpha, wl.w, y=y[b:b + 1],
+                            state=st.batch(b, b + 1))
+    torch.cuda.synchronize()
+    lizard_check_device_status()
+    y_ref, S_ref = O.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["mu"], inp["alpha"], wl.w, state=True)
+    assert rel_l2(y.cpu(), y_ref) <= TOL[q.dtype]
+    assert rel_l2(st.S.cpu(), S_ref) <= TOL[q.dtype]
+    assert torch.all(st.pos.cpu() == wl.L)
+    for p in range(wl.L - wl.w, wl.L):
+        assert torch.equal(st.ring_k[:, :, p % wl.w].cpu(), inp["k"][:, :, p])
