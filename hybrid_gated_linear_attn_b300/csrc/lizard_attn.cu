@@ -1,10 +1,10 @@
 // lizard_attn.cu -- C ABI of the Lizard hybrid attention operator.
 //
 // Host-side validation and launch of the kernels in decode.cuh,
-// prefill_ws.cuh (bf16, d = 128 or 64, w <= 65: warp-specialised tensor
-// cores, with the segment pre-pass of prefill_state.cuh for d = 128),
-// prefill_tc.cuh (bf16, d = 128, w > 65: tensor cores), prefill_simt.cuh
-// (fp32, and bf16 d = 64 with w > 65: CUDA cores, exact fp32), prefill_cont.cuh (start position of a continued prompt),
+// prefill_ws.cuh (bf16, d = 128 with any window, d = 64 with w <= 65:
+// warp-specialised tensor cores, with the segment pre-pass of
+// prefill_state.cuh for d = 128), prefill_simt.cuh (fp32, and bf16 d = 64
+// with w > 65: CUDA cores, exact fp32), prefill_cont.cuh (start position of a continued prompt),
 // backward_simt.cuh / backward_tc.cuh (gradients), gate_proj.cuh (the gate
 // projection) and the state initialiser below.  Declarations and the contract of every entry point are
 // in include/lizard_attn.h.
@@ -20,7 +20,6 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "prefill_simt.cuh"
-#include "prefill_tc.cuh"
 #include "prefill_ws.cuh"
 #include "prefill_state.cuh"
 #include "prefill_cont.cuh"
@@ -225,66 +224,22 @@ static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensor
     return launch_status();
 }
 
-// Lock-step tensor-core prefill (bf16, d = 128, 66 <= w <= 129).  Like the
-// warp-specialised one, a prompt from the empty state with few (batch, head)
-// units runs as sequence segments after the segment pre-pass; a continued
-// prompt runs unsegmented.
-static lizard_status launch_prefill_tc(const PrefillArgs &pa, cudaStream_t s)
-{
-    const int units = pa.B * pa.H, kv_units = pa.B * (pa.H / pa.group);
-    const int nchunks = (pa.L + tc::C - 1) / tc::C;
-    int nseg = pa.cont ? 1 : prefill_segments(units, nchunks);
-    if (nseg > nchunks) nseg = nchunks;
-    const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
-    nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
-    if (nseg < 1) nseg = 1;
-    CUtensorMap tq, tk, tv, tg;
-    if (!make_token_map(&tq, pa.q, units, pa.L) || !make_token_map(&tk, pa.k, kv_units, pa.L) ||
-        !make_token_map(&tv, pa.v, kv_units, pa.L) || !make_token_map(&tg, pa.g, units, pa.L))
-        return LIZARD_ERR_CUDA;
-    float *seg_states = nullptr;
-    if (nseg > 1 && scratch_alloc(reinterpret_cast<void **>(&seg_states), segment_states_bytes(units, nseg), s) !=
-                        cudaSuccess) {
-        cudaGetLastError();
-        nseg = 1;  // no scratch to be had: one CTA per unit walks the whole prompt
-    }
-    lizard_status rc = LIZARD_OK;
-    if (nseg > 1)
-        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, seg::ScanCont{}, pa.H,
-                                   pa.group, s);
-    tc::TcArgs ta{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
-                  static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),
-                  static_cast<__nv_bfloat16 *>(pa.y), pa.S_out, static_cast<__nv_bfloat16 *>(pa.ring_k),
-                  static_cast<__nv_bfloat16 *>(pa.ring_v), pa.pos, pa.alpha, pa.H, pa.L, pa.w, pa.m,
-                  (pa.w - 1 + tc::C - 1) / tc::C, pa.cont, pa.S0, pa.alpha_h, pa.group,
-                  seg_states, nseg > 1 ? seg_chunks : nchunks, nseg};
-    auto kern = ta.nprev == 0 ? tc::prefill_tc_kernel<0> : ta.nprev == 1 ? tc::prefill_tc_kernel<1>
-                                                                          : tc::prefill_tc_kernel<2>;
-    if (rc == LIZARD_OK) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES) !=
-            cudaSuccess)
-            rc = LIZARD_ERR_CUDA;
-        else {
-            kern<<<units * nseg, tc::THREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, ta);
-            rc = launch_status();
-        }
-    }
-    if (seg_states && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
-    return rc;
-}
-
-// Warp-specialised tensor-core prefill (bf16, d = 128 or 64, w <= 65).  With
-// few (batch, head) units and a long prompt the sequence (d = 128) is split
-// into segments that run side by side, after a pre-pass that computes every
-// segment's start state; `scratch` (nullable) holds those states, else they
-// live in stream-ordered scratch from the library's pool (freed on `s`).
-// d = 64 runs one CTA per unit on the same tiles, zero-padded.
+// Warp-specialised tensor-core prefill (bf16; d = 128, any window; d = 64,
+// w <= 65).  With few (batch, head) units and a long prompt the sequence
+// (d = 128) is split into segments that run side by side, after a pre-pass
+// that computes every segment's start state; `scratch` (nullable) holds
+// those states, else they live in stream-ordered scratch from the library's
+// pool (freed on `s`).  d = 64 runs one CTA per unit on the same tiles,
+// zero-padded.
 static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, float *scratch = nullptr,
                                        size_t scratch_bytes = 0, int force_segments = 0, int d = 128)
 {
     const int units = pa.B * pa.H;
     const int nchunks = (pa.L + ws::C - 1) / ws::C;
-    int nseg = d != ws::D ? 1 : force_segments > 0 ? force_segments : prefill_segments(units, nchunks);
+    // d = 64, and a continued prompt with a two-chunk band: one CTA per unit
+    // (the segment copies hold one chunk of window history)
+    const bool one_seg = d != ws::D || (pa.cont && pa.w > 65);
+    int nseg = one_seg ? 1 : force_segments > 0 ? force_segments : prefill_segments(units, nchunks);
     if (nseg > nchunks) nseg = nchunks;
     const int seg_chunks = (nchunks + nseg - 1) / (nseg > 0 ? nseg : 1);
     nseg = seg_chunks > 0 ? (nchunks + seg_chunks - 1) / seg_chunks : 1;  // no empty segment
@@ -334,8 +289,9 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
                   nseg > 1 ? seg_states : nullptr, nseg > 1 ? seg_chunks : nchunks, nseg,
                   pa.cont, seg0_state, hist, pa.alpha_h, pa.group};
     if (rc == LIZARD_OK)
-        rc = d == ws::D ? (pa.w == 1 ? launch_prefill_ws_np<0, ws::D>(tq, tk, tv, wa, units * nseg, s)
-                                     : launch_prefill_ws_np<1, ws::D>(tq, tk, tv, wa, units * nseg, s))
+        rc = d == ws::D ? (pa.w == 1   ? launch_prefill_ws_np<0, ws::D>(tq, tk, tv, wa, units * nseg, s)
+                           : pa.w <= 65 ? launch_prefill_ws_np<1, ws::D>(tq, tk, tv, wa, units * nseg, s)
+                                        : launch_prefill_ws_np<2, ws::D>(tq, tk, tv, wa, units * nseg, s))
                         : (pa.w == 1 ? launch_prefill_ws_np<0, 64>(tq, tk, tv, wa, units * nseg, s)
                                      : launch_prefill_ws_np<1, 64>(tq, tk, tv, wa, units * nseg, s));
     if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
@@ -673,7 +629,7 @@ lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v,
                    st ? st->pos : nullptr, 0, nullptr, alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == LIZARD_BF16)
-        return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
+        return dk == 128 ? launch_prefill_ws(pa, s)
                          : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
@@ -745,7 +701,7 @@ lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const
                    alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
-        return dk == 128 ? (w <= 65 ? launch_prefill_ws(pa, s) : launch_prefill_tc(pa, s))
+        return dk == 128 ? launch_prefill_ws(pa, s)
                          : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }

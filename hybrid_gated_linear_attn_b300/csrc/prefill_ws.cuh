@@ -1,5 +1,6 @@
 // prefill_ws.cuh -- chunked Lizard prefill on tcgen05 tensor cores as a
-// warp-specialised pipeline (bf16 inputs, d = 128 or 64, window w <= 65).
+// warp-specialised pipeline (bf16 inputs, d = 128 or 64, window w <= 129:
+// a band of up to two earlier chunks).
 //
 // Operator: gated linear attention (Lizard, gist.science/de section 2 item 1)
 // + anchor window with meta-memory sinks (item 2) + alpha combine (item 3).
@@ -73,7 +74,6 @@ constexpr int EPI_N = 128, PREP_N = 256, SOFT_N = 128;
 enum : int { NB_EPI = 1, NB_PREP = 2, NB_SOFT = 3, NB_EPI_R = 4, NB_PREP_R = 5, NB_SOFT_R = 6 };
 constexpr int META_ROWS = 16;
 constexpr int KROWS = C + META_ROWS;       // key tile rows: 64 tokens, then the meta keys
-constexpr int QS = 2;                      // q stages
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float SPAN2_MAX = 100.f;         // half-chunk decay span limit (base 2) of the GEMM path
 constexpr uint32_t WAIT_LIMIT = 1u << 21;
@@ -85,9 +85,13 @@ constexpr uint32_t SLOT = 2 * KB_K + 2 * KB_T;
 constexpr uint32_t SLOT_V = 2 * KB_K;      // v tile within a slot
 constexpr uint32_t OPB = 4 * KB_T;         // one operand buffer: QR tile, then KR tile
 constexpr int NVEC = 3;                    // per operand buffer: sig, tau, F (fp32 [128] each)
+// A band of NP earlier chunks.  NP <= 1: a k/v ring of NP + 2 slots (one
+// loads ahead) and two q stages.  NP = 2 (windows 66 .. 129): three slots
+// and one q stage, to fit shared memory.
 template <int NP>
 struct Smem {
-    static constexpr int NR = NP + 2;
+    static constexpr int NR = NP == 2 ? 3 : NP + 2;
+    static constexpr int QS = NP == 2 ? 1 : 2;    // q stages
     static constexpr uint32_t KV = 0;
     static constexpr uint32_t Q = KV + NR * SLOT;
     static constexpr uint32_t OP = Q + QS * 2 * KB_T;      // two operand buffers
@@ -95,7 +99,7 @@ struct Smem {
     static constexpr uint32_t VEC = W + (NP + 1) * KB_T;   // [2][NVEC][128], then tot[4][128] (fp32)
     static constexpr uint32_t FLAG = VEC + (2 * NVEC * 128 + 4 * 128) * 4;  // unsafe[2], abort
     static constexpr uint32_t BAR = FLAG + 16;
-    static constexpr int NBAR = 2 * QS + 4 * NR + 4 + 13;
+    static constexpr int NBAR = 2 * QS + 4 * NR + 4 + 14;
     static constexpr uint32_t TSLOT = BAR + NBAR * 8;
     static constexpr uint32_t USED = TSLOT + 16;
     static constexpr uint32_t BYTES = USED + 1024;
@@ -104,11 +108,13 @@ struct Smem {
 
 // Tensor-memory columns (512 allocated).
 constexpr uint32_t T_S = 0, T_S16 = 128, T_Y = 192, T_SC = 256;
+// With NP = 2 the intra-chunk scores A reuse the current chunk's score
+// columns: the A product waits until the softmax has read them.
 template <int NP>
 struct Tmem {
     static constexpr uint32_t SC_COLS = 64 * NP + 64 + META_ROWS;
-    static constexpr uint32_t A = T_SC + SC_COLS;
-    static_assert(A + 64 <= 512, "tensor memory budget");
+    static constexpr uint32_t A = NP == 2 ? T_SC + 64 * NP : T_SC + SC_COLS;
+    static_assert(A + 64 <= 512 && T_SC + SC_COLS <= 512, "tensor memory budget");
 };
 
 struct WsArgs {
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 {
     using SM = Smem<NP>;
     using TM = Tmem<NP>;
-    constexpr int NR = SM::NR;
+    constexpr int NR = SM::NR, QS = SM::QS;
     constexpr int NB = NP + 1;  // band chunks
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_align1024(smem_raw);
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *sc_full = op_free + 2, *a_full = sc_full + 1, *sc_free = sc_full + 2, *w_full = sc_full + 3,
              *w_free = sc_full + 4, *s_ready = sc_full + 5, *st_done = sc_full + 6, *s16_free = sc_full + 7,
              *y_full = sc_full + 8, *y_free = sc_full + 9, *drain = sc_full + 10, *drain_y = sc_full + 11,
-             *drain_s = sc_full + 12;
+             *drain_s = sc_full + 12, *sc_read = sc_full + 13;  // sc_read: NP = 2 only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + SM::TSLOT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&op_full[i], 1);
             mbar_init(&op_free[i], 2);   // A + state update, the readout
         }
-        for (int i = 0; i < 13; ++i) mbar_init(&sc_full[i], 1);
+        for (int i = 0; i < 14; ++i) mbar_init(&sc_full[i], 1);
         unsafe_f[0] = 0;
         unsafe_f[1] = 0;
         *abort_f = 0;
@@ -426,20 +432,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncthreads();
     }
     if (c_lo < 0) {
-        // Window history (chunk -1) into k/v slot 0, zero rows where no key,
-        // in the swizzled layout of a TMA-loaded tile.
+        // Window history (chunks c_lo .. -1) into k/v slots 0 .. -c_lo - 1,
+        // zero rows where no key, in the swizzled layout of a TMA-loaded
+        // tile.  (`hist` holds chunk -1 only: one earlier chunk.)
         const __nv_bfloat16 *rk = a.ring_k + (size_t)unit * w * d, *rv = a.ring_v + (size_t)unit * w * d;
         const __nv_bfloat16 *hk = a.hist ? a.hist + (size_t)unit * 2 * C * d : nullptr;
         const __nv_bfloat16 *hv = a.hist ? hk + C * d : nullptr;
         const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        for (int e = tid; e < C * (d / 8); e += THREADS) {
-            const int r = e / (d / 8), i8 = (e % (d / 8)) * 8;
-            const __nv_bfloat16 *kr = hk ? hk + (size_t)r * d : history_row(rk, p0, r - C, nvalid, w, d);
-            const __nv_bfloat16 *vr = hk ? hv + (size_t)r * d : history_row(rv, p0, r - C, nvalid, w, d);
+        for (int e = tid; e < -c_lo * C * (d / 8); e += THREADS) {
+            const int cc = e / (C * (d / 8)), r = (e / (d / 8)) % C, i8 = (e % (d / 8)) * 8;
+            const int tau = (c_lo + cc) * C + r;  // token position relative to the first new one
+            const __nv_bfloat16 *kr = hk ? hk + (size_t)r * d : history_row(rk, p0, tau, nvalid, w, d);
+            const __nv_bfloat16 *vr = hk ? hv + (size_t)r * d : history_row(rv, p0, tau, nvalid, w, d);
             const uint32_t sw = sw128_offset(r, (i8 % 64) * 2);
-            *reinterpret_cast<uint4 *>(sm + SM::KV + (i8 / 64) * KB_K + sw) =
-                kr ? *reinterpret_cast<const uint4 *>(kr + i8) : zero;
-            *reinterpret_cast<uint4 *>(sm + SM::KV + SLOT_V + (i8 / 64) * KB_T + sw) =
+            uint8_t *slot = sm + SM::KV + cc * SLOT;
+            *reinterpret_cast<uint4 *>(slot + (i8 / 64) * KB_K + sw) = kr ? *reinterpret_cast<const uint4 *>(kr + i8) : zero;
+            *reinterpret_cast<uint4 *>(slot + SLOT_V + (i8 / 64) * KB_T + sw) =
                 vr ? *reinterpret_cast<const uint4 *>(vr + i8) : zero;
         }
     }
@@ -458,6 +466,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // The band chunks before this CTA's first chunk (slots 0 .. c_begin -
+    // c_lo - 1, first use): loaded, or the window history in place.
+    auto preband_ready = [&](uint64_t *full) {
+        for (int i = 0; i < c_begin - c_lo; ++i)
+            if (!bwait(&full[i], 0, abort_f)) return false;
+        return true;
+    };
     bool failed = false;
     auto give_up = [&]() {
         failed = true;
@@ -534,7 +549,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int pc = c - c_begin, r = c - c_lo;
                 const int s = r % NR, qs = pc % QS;
                 const uint32_t qb = sb + SM::Q + qs * 2 * KB_T;
-                if ((pc == 0 && c_lo < c_begin && !bwait(&k_full[0], 0, abort_f)) ||
+                if ((pc == 0 && !preband_ready(k_full)) ||
                     !bwait(&k_full[s], r / NR, abort_f) || !bwait(&q_full[qs], pc / QS, abort_f) ||
                     (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) { give_up(); break; }
                 LZ_TRACE(pc, 24);
@@ -573,7 +588,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int pc = c - c_begin, r = c - c_lo, s = r % NR, b = pc & 1;
                 // intra-chunk decayed scores A (the A columns are free once the
                 // previous chunk's softmax has read them)
-                if (!bwait(&op_full[b], pc >> 1, abort_f) || (pc >= 1 && !bwait(sc_free, pc - 1, abort_f))) {
+                if (!bwait(&op_full[b], pc >> 1, abort_f) ||
+                    (NP == 2 ? !bwait(sc_read, pc, abort_f) : (pc >= 1 && !bwait(sc_free, pc - 1, abort_f)))) {
                     give_up();
                     break;
                 }
@@ -630,7 +646,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 LZ_TRACE(pc, 6);
                 // y^T += V_band^T W^T
                 if (!bwait(w_full, pc, abort_f) || !bwait(&v_full[r % NR], r / NR, abort_f) ||
-                    (pc == 0 && c_lo < c_begin && !bwait(&v_full[0], 0, abort_f))) { give_up(); break; }
+                    (pc == 0 && !preband_ready(v_full))) { give_up(); break; }
                 LZ_TRACE(pc, 25);
                 tc_fence_after();
 #pragma unroll 1
@@ -947,6 +963,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t rr[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(acc[e]);
+                    if constexpr (NP == 2) {
+                        // A lives in the current chunk's score columns: after the softmax read them
+                        if (!role_wait(warp == W_PREP, lane, NB_PREP_R, PREP_N,
+                                       [&] { return bwait(sc_read, pc, abort_f); })) { give_up(); break; }
+                        tc_fence_after();
+                    }
                     tmem_st16_x2<16>(tmem + tlane(quarter) + TM::A + 32 * ((warp - W_PREP) >> 2), rr);
                     tmem_wait_st();
                 }
@@ -1012,8 +1034,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Keys of row t: positions max(-nvalid, tg - w + 1) .. tg, i.e.
             // band columns lo .. hi.
             const int hi = t + 64 * NP, lo = max(-pbase - nvalid, hi - w + 1);
+            // (with NP = 2 the A product follows the read of the current
+            // chunk's scores, in their columns: waited for below)
             if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
-                           [&] { return bwait(sc_full, pc, abort_f) && bwait(a_full, pc, abort_f); })) {
+                           [&] { return bwait(sc_full, pc, abort_f) && (NP == 2 || bwait(a_full, pc, abort_f)); })) {
                 give_up();
                 break;
             }
@@ -1129,9 +1153,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2 + 16)) = make_uint4(pq[4], pq[5], pq[6], pq[7]);
                 }
             } else {
-                // Every band column scored separately (w = 65, or a window of
-                // one token), in three passes over tensor memory -- max, sum,
-                // weights -- so that one 16-column group is held at a time.
+                // Every band column scored separately (w = 65, a window of
+                // one token, or two earlier band chunks), in three passes over
+                // tensor memory -- max, sum, weights -- so that one 16-column
+                // group is held at a time.
                 const int d0 = 16 * hs - lo;
                 const uint32_t span = (uint32_t)(hi - lo);
                 uint32_t rm[16];
@@ -1179,8 +1204,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!brk) {
                     // W = alpha P / Z, plus A (s <= t) in the current chunk's columns
+                    constexpr int JW = NP == 2 ? 2 * NP : 2 * NB;  // groups done here
 #pragma unroll 1
-                    for (int jj = 0; jj < 2 * NB; ++jj) {
+                    for (int jj = 0; jj < JW; ++jj) {
                         const bool cur = jj >= 2 * NP;
                         uint32_t r[16], ra[16];
                         tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
@@ -1206,11 +1232,67 @@ __global__ void __launch_bounds__(THREADS, 1)
                         *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
                             make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
-                    // SC and A are read: the next chunk's scores may overwrite them
-                    tc_fence_before();
-                    named_bar(NB_SOFT, SOFT_N);
-                    if (st_ == 0) mbar_arrive(sc_free);
-                    LZ_TRACE(pc, 13);
+                    if constexpr (NP == 2) {
+                        // The current chunk: its weights to registers, its
+                        // columns released to the A product (A is accumulated
+                        // in them), then A added.
+                        float pv[2][16];
+#pragma unroll
+                        for (int jx = 0; jx < 2; ++jx) {
+                            const int jj = 2 * NP + jx;
+                            uint32_t r[16];
+                            tmem_ld16_x2<16>(tl + T_SC + 32 * jj, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                pv[jx][e] = (uint32_t)(d0 + 32 * jj + e) <= span
+                                                ? ex2(fmaf(__uint_as_float(r[e]), LOG2E, -M2)) * inv
+                                                : 0.f;
+                        }
+                        tc_fence_before();
+                        named_bar(NB_SOFT, SOFT_N);
+                        if (st_ == 0) mbar_arrive(sc_read);
+                        if (!role_wait(warp == W_SOFT, lane, NB_SOFT_R, SOFT_N,
+                                       [&] { return bwait(a_full, pc, abort_f); })) {
+                            give_up();
+                            brk = true;
+                        }
+                        if (!brk) {
+                            tc_fence_after();
+                            uint32_t ra[2][16];
+                            tmem_ld16_x2<16>(tl + TM::A, ra[0]);
+                            tmem_ld16_x2<16>(tl + TM::A + 32, ra[1]);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int jx = 0; jx < 2; ++jx) {
+                                const int col0 = 32 * (2 * NP + jx) + 16 * hs;
+                                uint32_t pk[8];
+#pragma unroll
+                                for (int e = 0; e < 16; e += 2) {
+                                    float wv[2];
+#pragma unroll
+                                    for (int u = 0; u < 2; ++u) {
+                                        float v = pv[jx][e + u];
+                                        if (col0 + e + u - 64 * NP <= t) v += __uint_as_float(ra[jx][e + u]);
+                                        wv[u] = rowok ? v : 0.f;
+                                    }
+                                    pk[e / 2] = f2_to_bf2(wv[0], wv[1]);
+                                }
+                                const uint32_t blk = (col0 / 64) * KB_T, byte = (col0 % 64) * 2;
+                                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte)) =
+                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                *reinterpret_cast<uint4 *>(sm + SM::W + blk + sw128_offset(t, byte + 16)) =
+                                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                            }
+                        }
+                    }
+                    if (!brk) {
+                        // SC and A are read: the next chunk's scores may overwrite them
+                        tc_fence_before();
+                        named_bar(NB_SOFT, SOFT_N);
+                        if (st_ == 0) mbar_arrive(sc_free);
+                        LZ_TRACE(pc, 13);
+                    }
                 }
             }
             if (brk) break;

@@ -57,8 +57,7 @@ def log2_sigmoid_ref(x):
     return torch.nn.functional.logsigmoid(xd) / torch.log(torch.tensor(2.0, dtype=torch.float64))
 
 
-@pytest.mark.parametrize("which,name", [(0, "polynomial"), (1, "ex2+lg2 pair"), (2, "ex2+lg2 lock-step"),
-                                        (3, "natural log")])
+@pytest.mark.parametrize("which,name", [(0, "polynomial"), (1, "ex2+lg2 pair"), (3, "natural log")])
 def test_log_sigmoid_forms(lib, which, name):
     x = grid()
     got = evaluate(lib, x, which).double()
@@ -94,6 +93,6 @@ def test_forms_agree_with_cuda_log2f(lib):
     ref = log2_sigmoid_ref(x)
     usable = (x.abs() <= 15) & torch.isfinite(cuda)
     assert float((cuda - ref).abs()[usable].max()) <= 1e-5
-    for which in (0, 1, 2):
+    for which in (0, 1):
         got = evaluate(lib, x, which).double()
         assert float((got - cuda).abs()[usable].max()) <= 2e-5, which
