@@ -647,7 +647,9 @@ lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const vo
         (m > 0 && !aligned16(meta_k)))
         return LIZARD_ERR_INVALID_ARG;
     // The variant covers the tensor-core prefill, the one with scratch.
-    if (dtype != LIZARD_BF16 || dk != 128 || dv != 128 || w > 65 || m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    if (dtype != LIZARD_BF16 || dk != dv || !((dk == 128 && w <= LIZARD_MAX_WINDOW) || (dk == 64 && w <= 65)) ||
+        m > LIZARD_MAX_META)
+        return LIZARD_ERR_UNSUPPORTED;
     if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
     if (st) {
         lizard_status rc = check_state(st);
@@ -664,7 +666,7 @@ lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const vo
                    st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
                    st ? st->pos : nullptr, 0, nullptr, nullptr, 1};
     // Segment states beyond LIZARD_NOALLOC_SCRATCH_BYTES: LIZARD_ERR_UNSUPPORTED, nothing launched.
-    return launch_prefill_ws(pa, (cudaStream_t)stream, scratch, LIZARD_NOALLOC_SCRATCH_BYTES);
+    return launch_prefill_ws(pa, (cudaStream_t)stream, scratch, LIZARD_NOALLOC_SCRATCH_BYTES, 0, dk);
 }
 
 lizard_status lizard_attn_prefill_continue(const void *q, const void *k, const void *v, const void *g,

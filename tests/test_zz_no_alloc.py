@@ -20,15 +20,22 @@ from hybrid_gated_linear_attn_b300.inputs import WORKLOADS, prefill_inputs, rel_
 
 pytestmark = pytest.mark.gpu
 
-def test_prefill_noalloc_matches_prefill_on_two_calls():
+# (window, head dim): one band chunk, two band chunks, head dim 64 (one
+# segment per unit: no scratch)
+CASES = [(48, 128), (100, 128), (64, 64)]
+
+
+@pytest.mark.parametrize("w,d", CASES, ids=[f"w{w}_d{d}" for w, d in CASES])
+def test_prefill_noalloc_matches_prefill_on_two_calls(w, d):
     B.build()
-    # Two (batch, head) units and 47 chunks: the prompt runs as 5 sequence
-    # segments, whose start states go through the scratch array.  The two
-    # calls use different inputs, so that anything left in the array by the
-    # first call would show in the second.  Both entry points run the same
-    # kernels with the same segment count, so the results are bit-identical.
+    # Two (batch, head) units and 47 chunks: the d = 128 prompt runs as 5
+    # sequence segments, whose start states go through the scratch array.
+    # The two calls use different inputs, so that anything left in the array
+    # by the first call would show in the second.  Both entry points run the
+    # same kernels with the same segment count, so the results are
+    # bit-identical.
     for call, seed in enumerate((123, 456)):
-        wl = WORKLOADS["llama3_8b"].replace(B=1, H=2, L=3000, w=48, seed=seed)
+        wl = WORKLOADS["llama3_8b"].replace(B=1, H=2, L=3000, w=w, dk=d, dv=d, seed=seed)
         inp = prefill_inputs(wl)
         q, k, v, g, mu = (inp[n].cuda() for n in ("q", "k", "v", "g", "mu"))
         st_ref = LizardState(wl.B, wl.H, wl.dk, wl.dv, wl.w, dtype=q.dtype)
