@@ -14,7 +14,8 @@
 //       reverse:  Ha[c] = dLoss/d(state after chunk c),
 //                 H <- diag(2^{b_last}) H + (q 2^{b})^T dy
 //   bwd_query_kernel     one CTA per (unit, chunk): the window softmax of the
-//       chunk's rows (log-normaliser, D_t = alpha dy_t . ya_t), dq, and
+//       chunk's rows (log-normaliser, D_t = alpha dy_t . ya_t, taken as
+//       alpha sum_s P_ts (dy v^T)_ts with P in fp32), dq, and
 //       q * dq_gate for dg, d mu and d alpha
 //   bwd_key_kernel       one CTA per (unit, chunk): dk and dv (gate terms
 //       from Ha[c], the anchor terms of this chunk's and the next chunk's
@@ -22,6 +23,12 @@
 //       chunks' share sum_j S_after[i][j] Ha[c][i][j] is regrouped (see E2)
 //       so that nothing cancels but fp32 rounding.
 // States and state gradients are kept in bf16, row = key dim.
+//
+// Head dim d = 64 (template DH) runs on the same 128-wide tiles: the dims
+// 64..127 of every input tile are cleared at the CTA's start and the TMA
+// loads only the first 64-dim box, so every product and state sees zeros
+// there; the scratch (states, q * dq_gate) keeps the 128-wide layout, and
+// only dims < d of dq, dk, dv, dg, d meta_k are written.
 #pragma once
 
 #include <type_traits>
@@ -46,6 +53,16 @@ constexpr int D = 128;
 constexpr int THREADS = 256;
 constexpr uint32_t TILE = C * 128;  // one 64-row x 128-byte swizzled block (8 KB)
 constexpr uint32_t WAIT = 1u << 21;
+
+// Clears the 64-dim blocks past the head dim of a CTA's input tiles (d = 64:
+// the TMA then loads only the first block of each).  `blk` lists the byte
+// offsets of those blocks (8 KB each, rows of 128 B).
+template <int N>
+__device__ __forceinline__ void clear_blocks(uint8_t *sm, const uint32_t (&blk)[N], uint32_t bytes)
+{
+    for (uint32_t e = threadIdx.x; e < N * (bytes / 16); e += blockDim.x)
+        *reinterpret_cast<uint4 *>(sm + blk[e / (bytes / 16)] + 16 * (e % (bytes / 16))) = make_uint4(0u, 0u, 0u, 0u);
+}
 
 // Bounded wait on an mbarrier phase by every thread of the CTA; false (and
 // the device error word set) on timeout.
@@ -142,6 +159,7 @@ constexpr uint32_t ST_SMEM = ST_TSLOT + 8 + 1024;
 // transposed in tensor memory (lane = value dim j, column = key dim i):
 //   store X (row i = key dim) to out[c]; X^T <- X^T diag(2^{b_last}) + y^T O,
 //   O = k 2^{b_last - b} (forward) or q 2^{b} (backward).
+template <int DH>
 __global__ void __launch_bounds__(THREADS, 2)
     chunk_states_kernel(const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq,
@@ -160,6 +178,12 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int L = a.L, nch = a.nchunks;
     const CUtensorMap *mx = rev ? &tq : &tk, *my = rev ? &tdy : &tv;
     __nv_bfloat16 *out = (rev ? a.Ha : a.Sb) + (size_t)unit * nch * D * D;
+    constexpr int d = DH, nbox = DH / 64;
+    if constexpr (DH < D) {
+        const uint32_t blk[4] = {TILE, 3 * TILE, ST_STAGE + TILE, ST_STAGE + 3 * TILE};  // x, y block 1 of both stages
+        clear_blocks(sm, blk, TILE);
+        fence_proxy_async_smem();
+    }
 
     if (warp == 0) {
         tmem_alloc(tslot, 128);
@@ -187,11 +211,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     auto issue = [&](int idx) {
         const int c = chunk_of(idx), s = idx & 1;
         uint8_t *st = sm + s * ST_STAGE;
-        mbar_arrive_expect_tx(&bar_tma[s], 2 * 2 * TILE);
-        tma_load_3d(st, mx, &bar_tma[s], 0, c * C, xyu);
-        tma_load_3d(st + TILE, mx, &bar_tma[s], 64, c * C, xyu);
-        tma_load_3d(st + 2 * TILE, my, &bar_tma[s], 0, c * C, xyu);
-        tma_load_3d(st + 3 * TILE, my, &bar_tma[s], 64, c * C, xyu);
+        mbar_arrive_expect_tx(&bar_tma[s], 2 * nbox * TILE);
+        for (int x = 0; x < nbox; ++x) {
+            tma_load_3d(st + x * TILE, mx, &bar_tma[s], 64 * x, c * C, xyu);
+            tma_load_3d(st + (2 + x) * TILE, my, &bar_tma[s], 64 * x, c * C, xyu);
+        }
     };
     if (tid == 0) issue(0);
     uint32_t tma_use[2] = {0, 0}, mma_use = 0, mma_issued = 0, tma_issued[2] = {1, 0};
@@ -199,14 +223,15 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int p = tid & 63, hq = tid >> 6;
     const uint32_t id_st = instr_desc(128, 128, FMT_BF16, 1, 1);
     // gate logits of dims 2p, 2p+1 for this thread's 16 tokens, one chunk ahead
-    const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * D) + p;
+    // (dims past d read as g = 0: their x and y are zero)
+    const uint32_t *gp = reinterpret_cast<const uint32_t *>(a.g + (size_t)unit * L * d) + p;
     uint32_t gnext[16];
     auto load_g = [&](int idx) {
         const int c = chunk_of(idx);
 #pragma unroll
         for (int tt = 0; tt < 16; ++tt) {
             const int row = c * C + 16 * hq + tt;
-            gnext[tt] = row < L ? gp[(size_t)row * (D / 2)] : 0u;
+            gnext[tt] = row < L && 2 * p < d ? gp[(size_t)row * (d / 2)] : 0u;
         }
     };
     load_g(0);
@@ -327,8 +352,7 @@ constexpr uint32_t QO_KP = QO_G + 2 * TILE;     // k of the previous chunk
 constexpr uint32_t QO_KC = QO_KP + 2 * TILE;    // k of this chunk + meta keys (80 rows, 2 blocks of KB_K)
 constexpr uint32_t QO_V = QO_KC + 2 * KB_K;     // v prev | v cur (4 blocks); later the state (128 x 128)
 constexpr uint32_t QO_KR = QO_V + 4 * TILE;     // k 2^{r - b}
-constexpr uint32_t QO_P = QO_KR + 2 * TILE;     // window probabilities [64][128 band] (bf16)
-constexpr uint32_t QO_DA = QO_P + 2 * TILE;     // tril(dy v^T) of this chunk [64][64]
+constexpr uint32_t QO_DA = QO_KR + 2 * TILE;    // tril(dy v^T) of this chunk [64][64]
 constexpr uint32_t QO_DSC = QO_DA + TILE;       // score gradients [64][prev 64 | cur 64 | meta 16]
 constexpr uint32_t QO_B = QO_DSC + 3 * TILE;    // b fp32 [64][128]
 constexpr uint32_t QO_VEC = QO_B + C * D * 4;   // r[128], tot[4][128], dC[64][16], flags
@@ -336,12 +360,13 @@ constexpr uint32_t QO_BAR = QO_VEC + (128 + 512 + 64 * 16 + 4) * 4;
 constexpr uint32_t QO_TSLOT = QO_BAR + 4 * 8;
 constexpr uint32_t QO_SMEM = QO_TSLOT + 8 + 1024;
 static_assert(QO_SMEM <= 232448, "shared memory budget");
-// Tensor-memory columns (512): window scores, dy v^T, then P V; later the
-// three parts of dq.
-constexpr uint32_t QT_SC = 0, QT_DP = 144, QT_YA = 272;
+// Tensor-memory columns (512): window scores, dy v^T; later the three parts
+// of dq.
+constexpr uint32_t QT_SC = 0, QT_DP = 144;
 constexpr uint32_t QT_G1 = 0, QT_G2 = 128, QT_DQA = 256;
 
 // grid = units * nchunks: CTA (unit, chunk c).
+template <int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_query_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -379,11 +404,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         flags[0] = 0;
         fence_mbar_init();
     }
-    // meta keys into rows 64..79 of the current key tile (zero past m)
+    constexpr int d = DH, nbox = DH / 64;
+    if constexpr (DH < D) {
+        // block 1 of q, dy, g, the keys (their 64 token rows), the values
+        const uint32_t blk[7] = {QO_Q + TILE, QO_DY + TILE, QO_G + TILE, QO_KP + TILE, QO_KC + KB_K, QO_V + TILE,
+                                 QO_V + 3 * TILE};
+        clear_blocks(sm, blk, TILE);
+    }
+    // meta keys into rows 64..79 of the current key tile (zero past m and d)
     for (int e = tid; e < META_ROWS * 64; e += THREADS) {
         const int r = e / 64, ip = e % 64, i = 2 * ip;
         uint32_t val = 0u;
-        if (r < m) val = *reinterpret_cast<const uint32_t *>(a.mu + ((size_t)h * m + r) * D + i);
+        if (r < m && i < d) val = *reinterpret_cast<const uint32_t *>(a.mu + ((size_t)h * m + r) * d + i);
         *reinterpret_cast<uint32_t *>(sm + QO_KC + (i / 64) * KB_K + sw128_offset(C + r, (i % 64) * 2)) = val;
     }
     fence_proxy_async_smem();
@@ -394,9 +426,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t mma_use = 0, mma_issued = 0, in_issued = 0, s_issued = 0;
 
     if (tid == 0) {
-        const uint32_t bytes = (has_prev ? 7 : 5) * 2 * TILE;
+        const uint32_t bytes = (has_prev ? 7 : 5) * nbox * TILE;
         mbar_arrive_expect_tx(bar_in, bytes);
-        for (int hb = 0; hb < 2; ++hb) {
+        for (int hb = 0; hb < nbox; ++hb) {
             tma_load_3d(sm + QO_Q + hb * TILE, &tq, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + QO_DY + hb * TILE, &tdy, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + QO_G + hb * TILE, &tg, bar_in, 64 * hb, c0, unit);
@@ -469,6 +501,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             ++mma_issued;
         }
         if (!mma_wait()) break;
+        // the value tiles are read (by dy v^T): load this chunk's state into their place
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_s, 4 * TILE);  // four 64 x 64 boxes
+            const int z = unit * nch + c;
+            for (int jb = 0; jb < 2; ++jb)
+                for (int ib = 0; ib < 2; ++ib)
+                    tma_load_3d(sm + QO_V + jb * 2 * TILE + ib * TILE, &tS, bar_s, 64 * jb, 64 * ib, z);
+            s_issued = 1;
+        }
         tc_fence_after();
         // ---- E1: row softmax (warps 0-3, row t, column half hs), tril(dA) (warps 4-7)
         const int quarter = warp & 3, hs = lane >> 4;
@@ -511,29 +552,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             lse2 = M2 + ws::lg2(sum);
             if (rowok && hs == 0) a.lse2[(size_t)unit * L + c0 + t] = lse2;
             if (hs == 0) tot[t] = lse2;  // for warps 4-7 (tot is free after the prep)
-            // P (bf16) for P V
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int col0 = 32 * jj + 16 * hs;
-                uint32_t pk[8];
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float pv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = col0 + e + u;
-                        pv[u] = (rowok && col >= lo && col <= hi)
-                                    ? ex2(fmaf(__uint_as_float(r[jj][e + u]), LOG2E, -lse2))
-                                    : 0.f;
-                    }
-                    pk[e / 2] = f2_to_bf2(pv[0], pv[1]);
-                }
-                const uint32_t o = QO_P + (col0 / 64) * TILE;
-                *reinterpret_cast<uint4 *>(sm + o + sw128_offset(t, (col0 % 64) * 2)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(sm + o + sw128_offset(t, (col0 % 64) * 2 + 16)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
         } else {
             uint32_t r[2][16];
             tmem_ld16_x2<16>(tl + QT_DP + 64, r[0]);
@@ -556,53 +574,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- M2: ya = P V_band
-        if (tid == 0) {
-            const uint32_t idv = instr_desc(64, 128, FMT_BF16, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                if (kk < 4 && !has_prev) continue;
-                const bool first = has_prev ? kk == 0 : kk == 4;
-                mma_bf16_ss(tmem + QT_YA, smem_desc(sb + QO_P + (kk / 4) * TILE + (kk % 4) * 32, 16, 1024),
-                            smem_desc(sb + QO_V + (kk / 4) * 2 * TILE + (kk % 4) * 2048, TILE, 1024), idv,
-                            first ? 0u : 1u);
-            }
-            mma_commit(bar_mma);
-            ++mma_issued;
-        }
-        if (!mma_wait()) break;
-        // the value tiles are read: load this chunk's state into their place
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_s, 4 * TILE);  // four 64 x 64 boxes
-            const int z = unit * nch + c;
-            for (int jb = 0; jb < 2; ++jb)
-                for (int ib = 0; ib < 2; ++ib)
-                    tma_load_3d(sm + QO_V + jb * 2 * TILE + ib * TILE, &tS, bar_s, 64 * jb, 64 * ib, z);
-            s_issued = 1;
-        }
         tc_fence_after();
         // ---- E2: D_t = alpha dy . ya, d alpha; score gradients; d mu.
+        // D_t = alpha sum_j dy_tj sum_s P_ts v_sj = alpha sum_s P_ts dP_ts
+        // with dP = dy v^T (the sinks carry no value): P in fp32, recomputed
+        // from the scores and the row's log-normaliser.
         // All eight warps: warp w takes rows 16 (w % 4) .. + 15 and the
         // column groups jj = 2 (w / 4), 2 (w / 4) + 1 (32 columns each).
         {
             const int g = warp >> 2;
             if (g == 1) lse2 = tot[t];
+            uint32_t rd[2][16];
+            float pr[2][16];
+            {
+                uint32_t r[2][16];
+#pragma unroll
+                for (int jx = 0; jx < 2; ++jx) {
+                    tmem_ld16_x2<16>(tl + QT_SC + 32 * (2 * g + jx), r[jx]);
+                    tmem_ld16_x2<16>(tl + QT_DP + 32 * (2 * g + jx), rd[jx]);
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int jx = 0; jx < 2; ++jx)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int col = 32 * (2 * g + jx) + 16 * hs + e;
+                        const bool valid = rowok && col >= lo && col <= hi;
+                        pr[jx][e] = valid ? ex2(fmaf(__uint_as_float(r[jx][e]), LOG2E, -lse2)) : 0.f;
+                    }
+            }
             float dot = 0.f;
 #pragma unroll
-            for (int jx = 0; jx < 2; ++jx) {
-                const int jj = 2 * g + jx;
-                uint32_t r[16];
-                tmem_ld16_x2<16>(tl + QT_YA + 32 * jj, r);
-                tmem_wait_ld();
-                const int j0 = 32 * jj + 16 * hs;
+            for (int jx = 0; jx < 2; ++jx)
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    const float2 dy2 = bf2_to_f2(*reinterpret_cast<const uint32_t *>(
-                        sm + QO_DY + (j0 / 64) * TILE + sw128_offset(t, ((j0 + e) % 64) * 2)));
-                    dot = fmaf(dy2.x, __uint_as_float(r[e]), dot);
-                    dot = fmaf(dy2.y, __uint_as_float(r[e + 1]), dot);
-                }
-            }
+                for (int e = 0; e < 16; ++e)
+                    dot = pr[jx][e] != 0.f ? fmaf(pr[jx][e], __uint_as_float(rd[jx][e]), dot) : dot;
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
             float *part = tot + 128;  // [2][64] row partials of the two column halves
             if (hs == 0) part[64 * g + t] = dot;
@@ -619,13 +625,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) atomicAdd(a.dalpha + (a.alpha_h ? h : 0), da);
             }
             // dSC = P (alpha dP - D_t) over the band, dC = P_meta (0 - D_t)
-            uint32_t r[2][16], rd[2][16];
-#pragma unroll
-            for (int jx = 0; jx < 2; ++jx) {
-                tmem_ld16_x2<16>(tl + QT_SC + 32 * (2 * g + jx), r[jx]);
-                tmem_ld16_x2<16>(tl + QT_DP + 32 * (2 * g + jx), rd[jx]);
-            }
-            tmem_wait_ld();
 #pragma unroll
             for (int jx = 0; jx < 2; ++jx) {
                 const int col0 = 32 * (2 * g + jx) + 16 * hs;
@@ -637,8 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int u = 0; u < 2; ++u) {
                         const int col = col0 + e + u;
                         const bool valid = rowok && col >= lo && col <= hi;
-                        const float pr = ex2(fmaf(__uint_as_float(r[jx][e + u]), LOG2E, -lse2));
-                        dv2[u] = valid ? pr * (alpha * __uint_as_float(rd[jx][e + u]) - Dt) : 0.f;
+                        dv2[u] = valid ? pr[jx][e + u] * (alpha * __uint_as_float(rd[jx][e + u]) - Dt) : 0.f;
                     }
                     pk[e / 2] = f2_to_bf2(dv2[0], dv2[1]);
                 }
@@ -676,8 +674,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         __syncthreads();
         // d mu[h][j][i] += sum_t dC[t][j] q[t][i]
-        for (int e = tid; e < m * D; e += THREADS) {
-            const int j = e / D, i = e % D;
+        for (int e = tid; e < m * d; e += THREADS) {
+            const int j = e / d, i = e % d;
             const uint8_t *qcol = sm + QO_Q + (i / 64) * TILE;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums over the tokens
             for (int t0 = 0; t0 < n; t0 += 4) {
@@ -689,7 +687,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                         qcol + sw128_offset(tt, (i % 64) * 2)));
                 }
             }
-            atomicAdd(&a.dmu[((size_t)h * m + j) * D + i], (acc[0] + acc[1]) + (acc[2] + acc[3]));
+            atomicAdd(&a.dmu[((size_t)h * m + j) * d + i], (acc[0] + acc[1]) + (acc[2] + acc[3]));
         }
         if (!cta_wait(bar_s, 0)) break;
         tc_fence_after();
@@ -791,9 +789,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 16; e += 2)
                     pk[e / 2] = f2_to_bf2(gate[e] + __uint_as_float(qa[e]), gate[e + 1] + __uint_as_float(qa[e + 1]));
-                uint4 *dqp = reinterpret_cast<uint4 *>(a.dq + row * D + i0);
-                dqp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dqp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                if (i0 < d) {
+                    uint4 *dqp = reinterpret_cast<uint4 *>(a.dq + row * d + i0);
+                    dqp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dqp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
                 float4 *xqp = reinterpret_cast<float4 *>(a.xq + row * D + i0);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) xqp[u] = make_float4(xg[4 * u], xg[4 * u + 1], xg[4 * u + 2], xg[4 * u + 3]);
@@ -849,6 +849,7 @@ static_assert(KO_SMEM <= 232448, "shared memory budget");
 constexpr uint32_t KT_SCC = 0, KT_DA = 64, KT_SCN = 128, KT_DPN = 192, KT_DKA = 256, KT_DV = 384;
 constexpr uint32_t KT_A = 0, KT_G1 = 0, KT_G2 = 128;
 
+template <int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_key_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -879,6 +880,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float alpha = head_alpha(a.alpha_h, a.alpha, unit % a.H);
     const int kvu = kv_unit(unit, a.H, a.group);
 
+    constexpr int d = DH, nbox = DH / 64;
+    if constexpr (DH < D) {
+        // block 1 of q, k, v, dy, g and of the next chunk's q, dy
+        const uint32_t blk[7] = {KO_Q + TILE, KO_K + TILE, KO_V + TILE, KO_DY + TILE, KO_G + TILE, KO_QN + TILE,
+                                 KO_DYN + TILE};
+        clear_blocks(sm, blk, TILE);
+        fence_proxy_async_smem();
+    }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -894,8 +903,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *tslot;
     uint32_t mma_use = 0, mma_issued = 0, in_issued = 0;
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar_in, (has_next ? 9 : 7) * 2 * TILE);
+        mbar_arrive_expect_tx(bar_in, ((has_next ? 7 : 5) * nbox + 4) * TILE);
         for (int hb = 0; hb < 2; ++hb) {
+            for (int ib = 0; ib < 2; ++ib)
+                tma_load_3d(sm + KO_H + hb * 2 * TILE + ib * TILE, &tH, bar_in, 64 * hb, 64 * ib, unit * nch + c);
+            if (hb >= nbox) continue;
             tma_load_3d(sm + KO_Q + hb * TILE, &tq, bar_in, 64 * hb, c0, unit);
             tma_load_3d(sm + KO_K + hb * TILE, &tk, bar_in, 64 * hb, c0, kvu);
             tma_load_3d(sm + KO_V + hb * TILE, &tv, bar_in, 64 * hb, c0, kvu);
@@ -905,8 +917,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_3d(sm + KO_QN + hb * TILE, &tq, bar_in, 64 * hb, c0 + C, unit);
                 tma_load_3d(sm + KO_DYN + hb * TILE, &tdy, bar_in, 64 * hb, c0 + C, unit);
             }
-            for (int ib = 0; ib < 2; ++ib)
-                tma_load_3d(sm + KO_H + hb * 2 * TILE + ib * TILE, &tH, bar_in, 64 * hb, 64 * ib, unit * nch + c);
         }
         in_issued = 1;
     }
@@ -1289,9 +1299,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     dkp[e / 2] = f2_to_bf2(dkv[e], dkv[e + 1]);
                     dvp[e / 2] = f2_to_bf2(__uint_as_float(vv[e]), __uint_as_float(vv[e + 1]));
                 }
-                if (rowok) {
-                    uint4 *dkq = reinterpret_cast<uint4 *>(a.dk + row * D + i0);
-                    uint4 *dvq = reinterpret_cast<uint4 *>(a.dv + row * D + i0);
+                if (rowok && i0 < d) {
+                    uint4 *dkq = reinterpret_cast<uint4 *>(a.dk + row * d + i0);
+                    uint4 *dvq = reinterpret_cast<uint4 *>(a.dv + row * d + i0);
                     dkq[0] = make_uint4(dkp[0], dkp[1], dkp[2], dkp[3]);
                     dkq[1] = make_uint4(dkp[4], dkp[5], dkp[6], dkp[7]);
                     dvq[0] = make_uint4(dvp[0], dvp[1], dvp[2], dvp[3]);
@@ -1340,7 +1350,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             for (int t2 = h1 - 1; t2 >= h0; --t2) {
                 run += bk[bx(t2, i)];
-                a.dg[((size_t)unit * L + c0 + t2) * D + i] = __float2bfloat16_rn((run + yo[bx(t2, i)]) * sg[t2 * D + i]);
+                if (i < d)
+                    a.dg[((size_t)unit * L + c0 + t2) * d + i] =
+                        __float2bfloat16_rn((run + yo[bx(t2, i)]) * sg[t2 * D + i]);
             }
         }
     } while (false);

@@ -402,6 +402,9 @@ static lizard_status launch_backward(BackwardArgs ba, float *dmu, float *dalpha,
 // Gradients on the tensor cores (bf16, d = 128, w <= 65): the chunk states
 // and state gradients, then the query-side and key-side kernels over every
 // (unit, chunk).  d mu and d alpha are accumulated, so they start at zero.
+// DH: the head dim (128, or 64 on the same zero-padded tiles); the scratch
+// keeps the 128-wide layout.
+template <int DH>
 static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, float *dalpha, cudaStream_t s)
 {
     const int units = ba.B * ba.H, L = ba.L, nch = (L + bwdtc::C - 1) / bwdtc::C;
@@ -411,7 +414,7 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     const size_t xq_bytes = (size_t)units * L * D * sizeof(float);
     const size_t row_bytes = ((size_t)units * L * sizeof(float) + 255) & ~(size_t)255;
     // grouped key/value heads: dk, dv per query head first, summed after
-    const size_t gqa_bytes = ba.group > 1 ? 2 * (size_t)units * L * D * sizeof(__nv_bfloat16) : 0;
+    const size_t gqa_bytes = ba.group > 1 ? 2 * (size_t)units * L * DH * sizeof(__nv_bfloat16) : 0;
     uint8_t *scratch = nullptr;
     if (scratch_alloc(reinterpret_cast<void **>(&scratch), 2 * st_bytes + xq_bytes + 2 * row_bytes + gqa_bytes, s) !=
         cudaSuccess) {
@@ -430,22 +433,22 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
     float *drow = reinterpret_cast<float *>(scratch + 2 * st_bytes + xq_bytes + row_bytes);
     lizard_status rc = LIZARD_OK;
     CUtensorMap tq, tk, tv, tg, tdy, tS, tH;
-    if (!make_token_map(&tq, ba.q, units, L) || !make_token_map(&tk, ba.k, kv_units, L) ||
-        !make_token_map(&tv, ba.v, kv_units, L) || !make_token_map(&tg, ba.g, units, L) ||
-        !make_token_map(&tdy, ba.dy, units, L) || !make_token_map(&tS, Sb, units * nch, (int)D) ||
+    if (!make_token_map(&tq, ba.q, units, L, DH) || !make_token_map(&tk, ba.k, kv_units, L, DH) ||
+        !make_token_map(&tv, ba.v, kv_units, L, DH) || !make_token_map(&tg, ba.g, units, L, DH) ||
+        !make_token_map(&tdy, ba.dy, units, L, DH) || !make_token_map(&tS, Sb, units * nch, (int)D) ||
         !make_token_map(&tH, Ha, units * nch, (int)D))
         rc = LIZARD_ERR_CUDA;
     if (rc == LIZARD_OK && cudaMemsetAsync(dalpha, 0, sizeof(float) * (ba.alpha_h ? ba.H : 1), s) != cudaSuccess)
         rc = LIZARD_ERR_CUDA;
-    if (rc == LIZARD_OK && dmu && cudaMemsetAsync(dmu, 0, sizeof(float) * ba.H * ba.m * D, s) != cudaSuccess)
+    if (rc == LIZARD_OK && dmu && cudaMemsetAsync(dmu, 0, sizeof(float) * ba.H * ba.m * DH, s) != cudaSuccess)
         rc = LIZARD_ERR_CUDA;
     if (rc == LIZARD_OK) {
         bwdtc::StatesArgs sa{Sb, Ha, static_cast<const __nv_bfloat16 *>(ba.g), L, nch, ba.H, ba.group};
-        if (cudaFuncSetAttribute(bwdtc::chunk_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bwdtc::chunk_states_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::ST_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
         else {
-            bwdtc::chunk_states_kernel<<<dim3(units, 2), bwdtc::THREADS, bwdtc::ST_SMEM, s>>>(tg, tk, tv, tq, tdy, sa);
+            bwdtc::chunk_states_kernel<DH><<<dim3(units, 2), bwdtc::THREADS, bwdtc::ST_SMEM, s>>>(tg, tk, tv, tq, tdy, sa);
             rc = launch_status();
         }
     }
@@ -453,26 +456,26 @@ static lizard_status launch_backward_tc(const BackwardArgs &ba, float *dmu, floa
         bwdtc::QueryArgs qa{static_cast<const __nv_bfloat16 *>(ba.mu), static_cast<const __nv_bfloat16 *>(ba.k),
                             static_cast<__nv_bfloat16 *>(ba.dq), xq, lse2, drow, dmu, dalpha, ba.alpha, ba.H, L,
                             ba.w, ba.m, nch, ba.alpha_h, ba.group};
-        if (cudaFuncSetAttribute(bwdtc::bwd_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bwdtc::bwd_query_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::QO_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
         else {
-            bwdtc::bwd_query_kernel<<<units * nch, bwdtc::THREADS, bwdtc::QO_SMEM, s>>>(tq, tk, tv, tg, tdy, tS, qa);
+            bwdtc::bwd_query_kernel<DH><<<units * nch, bwdtc::THREADS, bwdtc::QO_SMEM, s>>>(tq, tk, tv, tg, tdy, tS, qa);
             rc = launch_status();
         }
     }
     if (rc == LIZARD_OK) {
         bwdtc::KeyArgs ka{Sb, xq, lse2, drow, static_cast<__nv_bfloat16 *>(bg.dk), static_cast<__nv_bfloat16 *>(bg.dv),
                           static_cast<__nv_bfloat16 *>(ba.dg), ba.alpha, L, ba.w, nch, ba.alpha_h, ba.H, ba.group};
-        if (cudaFuncSetAttribute(bwdtc::bwd_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bwdtc::bwd_key_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bwdtc::KO_SMEM) != cudaSuccess)
             rc = LIZARD_ERR_CUDA;
         else {
-            bwdtc::bwd_key_kernel<<<units * nch, bwdtc::THREADS, bwdtc::KO_SMEM, s>>>(tq, tk, tv, tg, tdy, tH, ka);
+            bwdtc::bwd_key_kernel<DH><<<units * nch, bwdtc::THREADS, bwdtc::KO_SMEM, s>>>(tq, tk, tv, tg, tdy, tH, ka);
             rc = launch_status();
         }
     }
-    if (rc == LIZARD_OK && gqa_bytes) rc = launch_gqa_reduce<__nv_bfloat16, 128>(bg, ba.dk, ba.dv, s);
+    if (rc == LIZARD_OK && gqa_bytes) rc = launch_gqa_reduce<__nv_bfloat16, DH>(bg, ba.dk, ba.dv, s);
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -747,7 +750,8 @@ lizard_status lizard_attn_backward_v(const void *q, const void *k, const void *v
     BackwardArgs ba{q, k, v, g, meta_k, dy, dq, dk_out, dv_out, dg, alpha, B, H, L, w, m,
                     nullptr, nullptr, nullptr, nullptr, nullptr, alpha_h, group};
     float *dmu = m > 0 ? dmeta_k : nullptr;
-    if (dtype == LIZARD_BF16 && dk == 128 && w <= 65) return launch_backward_tc(ba, dmu, dalpha, s);
+    if (dtype == LIZARD_BF16 && w <= 65)
+        return dk == 128 ? launch_backward_tc<128>(ba, dmu, dalpha, s) : launch_backward_tc<64>(ba, dmu, dalpha, s);
     if (dtype == LIZARD_BF16)
         return dk == 128 ? launch_backward<__nv_bfloat16, 128>(ba, dmu, dalpha, s)
                          : launch_backward<__nv_bfloat16, 64>(ba, dmu, dalpha, s);

@@ -107,6 +107,16 @@ CASES = [
     ("tc_strong_decay", "bf16", 1, 2, 256, 128, 64, 8, 0.0, 2.0, 0.5),
     ("tc_open_gates", "bf16", 1, 2, 200, 128, 32, 4, 12.0, 0.5, 1.0),
     ("tc_many_units", "bf16", 3, 8, 130, 128, 64, 4, 3.0, 1.0, 1.0),
+    # tensor-core path with head dim 64 (tiles zero-padded to 128)
+    ("tc_d64_w64", "bf16", 2, 2, 200, 64, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_d64_one_chunk", "bf16", 2, 2, 64, 64, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_d64_single_token", "bf16", 1, 2, 1, 64, 64, 4, 3.0, 1.0, 1.0),
+    ("tc_d64_window_one", "bf16", 1, 2, 190, 64, 1, 3, 3.0, 1.0, 1.0),
+    ("tc_d64_wide_span_exact", "bf16", 1, 2, 300, 64, 64, 4, -8.0, 4.0, 1.0),
+    ("tc_d64_no_meta", "bf16", 1, 2, 200, 64, 32, 0, 3.0, 1.0, 1.0),
+    ("tc_d64_window_65_max_meta", "bf16", 1, 2, 260, 64, 65, 16, 3.0, 1.0, 1.0),
+    ("tc_d64_alpha_zero", "bf16", 1, 2, 150, 64, 64, 4, 3.0, 1.0, 0.0),
+    ("tc_d64_open_gates", "bf16", 1, 2, 200, 64, 32, 4, 12.0, 0.5, 1.0),
 ]
 
 
@@ -148,3 +158,9 @@ def test_decay_stress_full_size_all_units():
     """B2 H32 L8192 d128 bf16, g ~ N(0, 2), w128 m8 alpha 0.5 (w > 65: the
     exact CUDA-core path), all 64 units."""
     _full_size("decay_stress", 98)
+
+
+def test_d64_full_size_all_units():
+    """B4 H32 L4096 d64 bf16 (the tensor-core path on zero-padded tiles),
+    all 128 units."""
+    _full_size("d64", 97)

@@ -118,6 +118,7 @@ def test_continue_and_decode_variants(dt, d, w):
 BWD_CASES = [
     # name, dtype, B, H, Hkv, L, d, w, m
     ("bwd_tc_gqa2", "bf16", 1, 4, 2, 200, 128, 64, 4),
+    ("bwd_tc_d64_gqa2", "bf16", 1, 4, 2, 200, 64, 64, 4),
     ("bwd_tc_mqa", "bf16", 2, 2, 1, 130, 128, 33, 2),
     ("bwd_simt_f32_gqa2", "f32", 1, 4, 2, 120, 64, 16, 4),
     ("bwd_simt_bf16_w100", "bf16", 1, 4, 2, 150, 128, 100, 4),
