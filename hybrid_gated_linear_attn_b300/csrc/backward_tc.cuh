@@ -281,22 +281,28 @@ __global__ void __launch_bounds__(THREADS, 2)
             ++tma_issued[(idx + 1) & 1];
         }
         tc_fence_after();
-        if (warp < 4) {
-            // store X (this chunk's entry), then decay it
-            const int j = 32 * warp + lane;
+        {
+            // store X (this chunk's entry), then decay it: warp w takes
+            // lanes 32 (w % 4) .. + 31 and columns 64 (w / 4) .. + 63
+            const int q4 = warp & 3, ch = warp >> 2;
+            const int j = 32 * q4 + lane;
             __nv_bfloat16 *o = out + (size_t)c * D * D + j;
 #pragma unroll 1
-            for (int cc = 0; cc < D; cc += 16) {
-                uint32_t r[16];
-                tmem_ld16(tmem + tlane(warp) + cc, r);
+            for (int cc = 64 * ch; cc < 64 * ch + 64; cc += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tmem + tlane(q4) + cc, r0);
+                tmem_ld16(tmem + tlane(q4) + cc + 16, r1);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float x = __uint_as_float(r[e]);
-                    o[(size_t)(cc + e) * D] = __float2bfloat16_rn(x);
-                    r[e] = __float_as_uint(x * dec[cc + e]);
+                    const float x0 = __uint_as_float(r0[e]), x1 = __uint_as_float(r1[e]);
+                    o[(size_t)(cc + e) * D] = __float2bfloat16_rn(x0);
+                    o[(size_t)(cc + 16 + e) * D] = __float2bfloat16_rn(x1);
+                    r0[e] = __float_as_uint(x0 * dec[cc + e]);
+                    r1[e] = __float_as_uint(x1 * dec[cc + 16 + e]);
                 }
-                tmem_st16(tmem + tlane(warp) + cc, r);
+                tmem_st16(tmem + tlane(q4) + cc, r0);
+                tmem_st16(tmem + tlane(q4) + cc + 16, r1);
             }
             tmem_wait_st();
         }
