@@ -54,6 +54,18 @@ constexpr int THREADS = 256;
 constexpr uint32_t TILE = C * 128;  // one 64-row x 128-byte swizzled block (8 KB)
 constexpr uint32_t WAIT = 1u << 21;
 
+// A 16-byte global load issued where it is written: volatile, so the
+// compiler keeps it ahead of the waits that follow instead of sinking it to
+// its first use (a prefetch meant to overlap them).
+__device__ __forceinline__ uint4 ldg_early(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // Clears the 64-dim blocks past the head dim of a CTA's input tiles (d = 64:
 // the TMA then loads only the first block of each).  `blk` lists the byte
 // offsets of those blocks (8 KB each, rows of 128 B).
@@ -953,7 +965,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint4 *Sp = reinterpret_cast<const uint4 *>(a.Sb + ((size_t)unit * nch + c) * D * D +
                                                           (size_t)(tid & 127) * D + 64 * (tid >> 7));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) sv[u] = Sp[u];
+        for (int u = 0; u < 8; ++u) sv[u] = ldg_early(Sp + u);
     }
     int unsafe = 0;
     do {
@@ -1203,14 +1215,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // q * dq_gate of this thread's row and columns, fetched while the
         // gate products run
-        float4 xq4[2][4];
+        uint4 xq4[2][4];
         if (t < n) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const float4 *xp = reinterpret_cast<const float4 *>(
                     a.xq + ((size_t)unit * L + c0 + t) * D + 64 * (warp >> 2) + 32 * jj + 16 * hs);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) xq4[jj][u] = xp[u];
+                for (int u = 0; u < 4; ++u) xq4[jj][u] = ldg_early(xp + u);
             }
         }
         if (!mma_wait()) break;
@@ -1237,11 +1249,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (rowok) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float4 x4 = xq4[jj][u];
-                        xqv[4 * u] = x4.x;
-                        xqv[4 * u + 1] = x4.y;
-                        xqv[4 * u + 2] = x4.z;
-                        xqv[4 * u + 3] = x4.w;
+                        const uint4 x4 = xq4[jj][u];
+                        xqv[4 * u] = __uint_as_float(x4.x);
+                        xqv[4 * u + 1] = __uint_as_float(x4.y);
+                        xqv[4 * u + 2] = __uint_as_float(x4.z);
+                        xqv[4 * u + 3] = __uint_as_float(x4.w);
                     }
                 }
                 tmem_ld16_x2<16>(tl + KT_G1 + cofs, g1);
