@@ -369,7 +369,7 @@ def run_ours(args, world, rank, local):
         pflops = 2.0 * Bl * wl.L * wl.H * wl.dk * dmodel
 
         # ---- the decay-stress and long-context prefill workloads, same run ----
-        extra = {}
+        extra, extra_bwd = {}, {}
         for name in ("decay_stress", "long_context", "d64"):
             xwl = WORKLOADS[name]
             xin = prefill_inputs(xwl, seed=rank_seed(xwl.seed, rank))
@@ -383,6 +383,16 @@ def run_ours(args, world, rank, local):
             xsteps = max(3, min(args.steps, 10))
             xms = max_over_ranks(time_loop(xstep, xsteps, max(args.warmup, 2), stream), world)
             extra[name] = (xwl, xms, xsteps)
+            if name == "d64":  # its backward too (the tensor-core path on zero-padded tiles)
+                xdy = torch.randn(xq.shape, generator=torch.Generator().manual_seed(rank_seed(xwl.seed + 11, rank)))
+                xdy = xdy.to(xq.dtype).cuda()
+
+                def xbstep():
+                    lizard_attn_backward(xq, xk, xv, xg, xmu, xwl.alpha, xwl.w, xdy, stream=stream)
+
+                xbms = max_over_ranks(time_loop(xbstep, xsteps, max(args.warmup, 2), stream), world)
+                extra_bwd[name] = (xwl, xbms, xsteps)
+                del xdy
             del xq, xk, xv, xg, xmu, xy, xst, xin
     lizard_check_device_status(stream)
     clock = clocks.summary()
@@ -482,6 +492,16 @@ def run_ours(args, world, rank, local):
                                 "algorithmic_bytes": prefill_bytes(xwl)},
                    "tensor_frac": prefill_flops(xwl) / (xms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
             for name, (xwl, xms, xsteps) in extra.items()},
+        "backward_workloads": {
+            name: {"workload": f"{name} backward B{xwl.B} H{xwl.H} L{xwl.L} d{xwl.dk} w{xwl.w} m{xwl.m} {xwl.dtype}",
+                   "value": world * xwl.B * xwl.L / (xms * 1e-3), "unit": "tokens/s", "ms_per_step": xms,
+                   "steps": xsteps,
+                   "roofline": {"bound": "hbm", "achieved": backward_bytes(xwl) / (xms * 1e-3) / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": backward_bytes(xwl) / (xms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "peak_source": peak_src, "traffic": None, "launch_ms": xms,
+                                "algorithmic_bytes": backward_bytes(xwl)}}
+            for name, (xwl, xms, xsteps) in extra_bwd.items()},
         "e2e": {"value": world * tokens_rank / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * 1,
