@@ -344,6 +344,21 @@ def run_ours(args, world, rank, local):
         dms = time_loop(dstep, dsteps, max(args.warmup, 3), stream)
         dms = max_over_ranks(dms, world)
         dlaunch_ms = dms  # one kernel per decode step: the timed average is its duration
+        # The same steps alternating between two states (2 x 134 MB, above
+        # L2): no step finds the state it updates left in L2 by the one before.
+        dst2 = LizardState(dwl.B, dwl.H, dwl.dk, dwl.dv, dwl.w, dtype=torch.bfloat16)
+        for n in ("S", "ring_k", "ring_v", "pos"):
+            getattr(dst2, n).copy_(getattr(dst, n))
+        states = (dst, dst2)
+
+        def dstep2():
+            p = pool[ctr[0] % len(pool)]
+            st_ = states[ctr[0] % 2]
+            ctr[0] += 1
+            lizard_attn_decode_step(p["q"], p["k"], p["v"], p["g"], dmu, dwl.alpha, st_, y=dy, stream=stream)
+
+        dms2 = max_over_ranks(time_loop(dstep2, dsteps, max(args.warmup, 3), stream), world)
+        del dst2, states
 
         # ---- backward of the prefill (training), same run ----
         gen = torch.Generator().manual_seed(rank_seed(wl.seed + 11, rank))
@@ -464,7 +479,11 @@ def run_ours(args, world, rank, local):
                    "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": d_gbs / peaks["hbm_gbs"], "peak_source": peak_src,
                                 "traffic": ncu_traffic("decode", DECODE_KERNEL_SRC),
-                                "launch_ms": dlaunch_ms, "algorithmic_bytes": d_nbytes}},
+                                "launch_ms": dlaunch_ms, "algorithmic_bytes": d_nbytes},
+                   "rotating_states": {"ms_per_step": dms2, "value": world * dwl.B / (dms2 * 1e-3),
+                                       "achieved_gbs": d_nbytes / (dms2 * 1e-3) / 1e9,
+                                       "frac": d_nbytes / (dms2 * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                       "note": "two states in turn: no step reads a state left in L2"}},
         "backward": {"value": world * tokens_rank / (bms * 1e-3), "unit": "tokens/s", "ms_per_step": bms,
                      "steps": bsteps,
                      "train_value": world * tokens_rank / ((ms + bms) * 1e-3),
