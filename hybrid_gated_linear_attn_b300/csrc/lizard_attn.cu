@@ -169,7 +169,9 @@ template <int NP, int DH>
 static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                           const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
-    auto kern = ws::prefill_ws_kernel<NP, DH>;
+    // w <= 64 with one earlier band chunk: the instance with only the
+    // one-overlay softmax compiled in
+    auto kern = NP == 1 && wa.w <= 64 ? ws::prefill_ws_kernel<NP, DH, true> : ws::prefill_ws_kernel<NP, DH, false>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;

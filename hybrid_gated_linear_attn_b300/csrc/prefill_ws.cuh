@@ -343,7 +343,9 @@ __device__ __forceinline__ void mma_chain(uint32_t d, uint64_t da, uint64_t db, 
     }
 }
 
-template <int NP, int DH>
+// FAST: the window fits one 64-slot overlay (NP = 1, w <= 64): only that
+// softmax is compiled in, which keeps the chunk loop's code small.
+template <int NP, int DH, bool FAST = false>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const WsArgs a)
@@ -1048,8 +1050,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Row t's window keys all sit in distinct slots (exactly the 64
             // slots when w = 64 and the history is complete), so each thread
             // scores 32 slots, not 64.
-            bool brk = false, fast = false;
-            if constexpr (NP == 1) fast = w <= 64;
+            bool brk = false, fast = FAST;
+            if constexpr (NP == 1 && !FAST) fast = w <= 64;
             if (fast) {
                 // Read SC and A first and release their columns at once, so
                 // that the next chunk's score products overlap this softmax.
@@ -1152,7 +1154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2)) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
                     *reinterpret_cast<uint4 *>(sm + SM::W + KB_T + sw128_offset(t, col * 2 + 16)) = make_uint4(pq[4], pq[5], pq[6], pq[7]);
                 }
-            } else {
+            } else if constexpr (!FAST) {
                 // Every band column scored separately (w = 65, a window of
                 // one token, or two earlier band chunks), in three passes over
                 // tensor memory -- max, sum, weights -- so that one 16-column
