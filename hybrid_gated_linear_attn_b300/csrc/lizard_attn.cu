@@ -171,7 +171,9 @@ static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorM
 {
     // w <= 64 with one earlier band chunk: the instance with only the
     // one-overlay softmax compiled in
-    auto kern = NP == 1 && wa.w <= 64 ? ws::prefill_ws_kernel<NP, DH, true> : ws::prefill_ws_kernel<NP, DH, false>;
+    auto kern = ws::prefill_ws_kernel<NP, DH, false>;
+    if constexpr (NP == 1)
+        if (wa.w <= 64) kern = ws::prefill_ws_kernel<NP, DH, true>;
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
