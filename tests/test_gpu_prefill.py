@@ -75,6 +75,13 @@ CASES = [
     ("segments_w100", "bf16", 1, 2, 2000, 128, 100, 4, 3.0, 1.0, 1.0),
     ("segments_w128_strong_decay", "bf16", 1, 2, 2100, 128, 128, 8, 0.0, 2.0, 0.5),
     ("segments_w66_exact_intra", "bf16", 1, 1, 1500, 128, 66, 2, -8.0, 4.0, 1.0),
+    # windows 66..128: two earlier band chunks (small prompts, one segment)
+    ("w100_single_token", "bf16", 2, 2, 1, 128, 100, 4, 3.0, 1.0, 1.0),
+    ("w128_L_below_w", "bf16", 2, 2, 40, 128, 128, 4, 3.0, 1.0, 1.0),
+    ("w128_two_chunks", "bf16", 1, 3, 128, 128, 128, 8, 3.0, 1.0, 0.5),
+    ("w97_ragged_no_meta", "bf16", 1, 2, 333, 128, 97, 0, 3.0, 1.0, 1.0),
+    ("w128_alpha_zero_open_gates", "bf16", 1, 2, 300, 128, 128, 4, 12.0, 0.5, 0.0),
+    ("w120_more_units_than_sms", "bf16", 5, 32, 70, 128, 120, 4, 3.0, 1.0, 1.0),
     # head dim 64 on the tensor-core pipeline (tiles zero-padded to 128)
     ("d64_window_one", "bf16", 1, 2, 150, 64, 1, 3, 3.0, 1.0, 1.0),
     ("d64_window_65", "bf16", 1, 2, 333, 64, 65, 4, 3.0, 1.0, 1.0),
