@@ -1134,15 +1134,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const float2 inv2 = make_float2(rowok ? inv : 0.f, rowok ? inv : 0.f);
-#pragma unroll
+                // (a rolled loop: jj picks registers by value, so the code is
+                // one copy of the body)
+#pragma unroll 1
                 for (int jj = 0; jj < 2; ++jj) {
                     const int dj = t - 16 * hs - 32 * jj;
                     uint32_t pp[8], pq[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        const float2 v = mul2(make_float2(x[jj][e], x[jj][e + 1]), inv2);
-                        const float2 av = make_float2(rowok ? __uint_as_float(ra2[jj][e]) : 0.f,
-                                                      rowok ? __uint_as_float(ra2[jj][e + 1]) : 0.f);
+                        const float x0 = jj ? x[1][e] : x[0][e], x1 = jj ? x[1][e + 1] : x[0][e + 1];
+                        const uint32_t a0 = jj ? ra2[1][e] : ra2[0][e], a1 = jj ? ra2[1][e + 1] : ra2[0][e + 1];
+                        const float2 v = mul2(make_float2(x0, x1), inv2);
+                        const float2 av = make_float2(rowok ? __uint_as_float(a0) : 0.f,
+                                                      rowok ? __uint_as_float(a1) : 0.f);
                         const float2 vc = add2(v, av);
                         const bool c0_ = e <= dj, c1_ = e + 1 <= dj;
                         pp[e / 2] = f2_to_bf2(c0_ ? 0.f : v.x, c1_ ? 0.f : v.y);
