@@ -786,7 +786,8 @@ lizard_status lizard_gate_projection(const void *x, const void *w_gamma, int B, 
     const uint32_t smem = nh == 2 ? gproj::Cfg<2>::SMEM : gproj::Cfg<1>::SMEM;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<(unsigned)tiles, gproj::THREADS, smem, (cudaStream_t)stream>>>(tx, tw, ga);
+    const int64_t ctas = tiles < sm_count() ? tiles : sm_count();  // persistent: one CTA per SM
+    kern<<<(unsigned)ctas, gproj::THREADS, smem, (cudaStream_t)stream>>>(tx, tw, ga);
     return launch_status();
 }
 
