@@ -715,17 +715,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool odd = lane & 1;
             __nv_bfloat16 *yq = yp - (odd ? 1 : 0) + (odd ? d : 0);
             const int t_odd = odd ? 1 : 0;
+            uint32_t pk[4][8];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
+                for (int e = 0; e < 16; e += 2)
+                    pk[q4][e / 2] = f2_to_bf2(__uint_as_float(r[q4][e]), __uint_as_float(r[q4][e + 1]));
+            // rolled over the four 16-token groups: pk shifts down by one
+            // group per pass (static register indices)
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
                 for (int e = 0; e < 16; e += 2) {
-                    const uint32_t mine = f2_to_bf2(__uint_as_float(r[q4][e]), __uint_as_float(r[q4][e + 1]));
+                    const uint32_t mine = pk[0][e / 2];
                     const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
                     // even: (mine.lo, other.lo); odd: (other.hi, mine.hi)
                     const uint32_t out = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
                     if (live && 16 * q4 + e + t_odd < n)
                         *reinterpret_cast<uint32_t *>(yq + (size_t)(16 * q4 + e) * d) = out;
                 }
+#pragma unroll
+                for (int g4 = 0; g4 < 3; ++g4)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) pk[g4][e] = pk[g4 + 1][e];
+            }
             LZ_TRACE(py, 11);
             return true;
         };
@@ -882,16 +895,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // QR = q / Z; every factor lies in [2^-SPAN2_MAX, 2^SPAN2_MAX].
                 const float2 er = make_float2(rcp(h0.x), rcp(h0.y));     // 2^r
                 float2 R = hq == 0 ? er : hq == 1 ? mul2(er, T[0]) : hq == 2 ? make_float2(1.f, 1.f) : T[2];
+                // rolled over blocks of four tokens, iv shifting down by four
+                // per block (static register indices): one copy of the body
+                // keeps the chunk loop's code small
                 if (live)
+#pragma unroll 1
+                for (int t4 = 0; t4 < 16; t4 += 4) {
 #pragma unroll
-                for (int tt = 0; tt < 16; ++tt) {
-                    R = mul2(R, iv[tt]);
-                    const uint32_t off = sw128_offset(16 * hq + tt, kbyte);
-                    const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
-                    const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
-                    const float2 kr = mul2(kv, R), qr = mul2(qv, make_float2(rcp(R.x), rcp(R.y)));
-                    *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
-                    *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
+                    for (int i = 0; i < 4; ++i) {
+                        R = mul2(R, iv[i]);
+                        const uint32_t off = sw128_offset(16 * hq + t4 + i, kbyte);
+                        const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kraw + off));
+                        const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qraw + off));
+                        const float2 kr = mul2(kv, R), qr = mul2(qv, make_float2(rcp(R.x), rcp(R.y)));
+                        *reinterpret_cast<uint32_t *>(kr_t + off) = f2_to_bf2(kr.x, kr.y);
+                        *reinterpret_cast<uint32_t *>(qr_t + off) = f2_to_bf2(qr.x, qr.y);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 12; ++i) iv[i] = iv[i + 4];
                 }
                 const float2 F = make_float2(rcp(h1.x), rcp(h1.y));       // 2^{b_last - r}
                 const float2 sc = mul2(Fp, er);                              // F_{c-1} 2^r
