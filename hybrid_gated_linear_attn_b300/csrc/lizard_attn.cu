@@ -170,10 +170,15 @@ static lizard_status launch_prefill_ws_np(const CUtensorMap &tq, const CUtensorM
                                           const ws::WsArgs &wa, int ctas, cudaStream_t s)
 {
     // w <= 64 with one earlier band chunk: the instance with only the
-    // one-overlay softmax compiled in
+    // one-overlay softmax compiled in; w = 64 from the empty state: the one
+    // without the masked selection either
     auto kern = ws::prefill_ws_kernel<NP, DH, false>;
-    if constexpr (NP == 1)
-        if (wa.w <= 64) kern = ws::prefill_ws_kernel<NP, DH, true>;
+    if constexpr (NP == 1) {
+        if (wa.w == 64 && !wa.cont)
+            kern = ws::prefill_ws_kernel<NP, DH, true, true>;
+        else if (wa.w <= 64)
+            kern = ws::prefill_ws_kernel<NP, DH, true>;
+    }
     constexpr uint32_t smem = ws::Smem<NP>::BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;

@@ -344,8 +344,12 @@ __device__ __forceinline__ void mma_chain(uint32_t d, uint64_t da, uint64_t db, 
 }
 
 // FAST: the window fits one 64-slot overlay (NP = 1, w <= 64): only that
-// softmax is compiled in, which keeps the chunk loop's code small.
-template <int NP, int DH, bool FAST = false>
+// softmax is compiled in, which keeps the chunk loop's code small.  W64
+// (with FAST): w = 64 and a prompt from the empty state, so that every slot
+// of the overlay is a key of its row -- in the first chunk the missing
+// earlier chunk's score columns hold -inf -- and the masked selection is
+// left out as well.
+template <int NP, int DH, bool FAST = false, bool W64 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_ws_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const WsArgs a)
@@ -1049,6 +1053,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tl = tmem + tlane(quarter);
         const int st_ = tid - W_SOFT * 32;
         const float alpha = head_alpha(a.alpha_h, a.alpha, h);  // this head's anchor weight
+        if constexpr (W64) {
+            if (c_lo == c_begin) {
+                // no chunk before the first: its score columns read as no
+                // key (no product writes them before the first release)
+                uint32_t ninf[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ninf[e] = 0xFF800000u;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 16) tmem_st16(tl + T_SC + cc, ninf);
+                tmem_wait_st();
+            }
+        }
         for (int c = c_begin; c < c_end; ++c) {
             const int pc = c - c_begin;
             const int c0 = c * C, n = min(C, L - c0);
@@ -1087,7 +1103,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld16_x2<16>(tl + T_SC + 96, rc[1]);
                     tmem_ld16(tl + T_SC + 128, rm);
                     tmem_wait_ld();
-                    if (w == 64 && 64 - c0 - nvalid <= 1) {
+                    if (W64 || (w == 64 && 64 - c0 - nvalid <= 1)) {
                         // every slot is a key of its row
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {

@@ -82,6 +82,11 @@ CASES = [
     ("w97_ragged_no_meta", "bf16", 1, 2, 333, 128, 97, 0, 3.0, 1.0, 1.0),
     ("w128_alpha_zero_open_gates", "bf16", 1, 2, 300, 128, 128, 4, 12.0, 0.5, 0.0),
     ("w120_more_units_than_sms", "bf16", 5, 32, 70, 128, 120, 4, 3.0, 1.0, 1.0),
+    # w = 64 from the empty state (the instance without the masked
+    # selection: the first chunk's missing earlier chunk scores as -inf)
+    ("w64_single_token", "bf16", 2, 2, 1, 128, 64, 4, 3.0, 1.0, 1.0),
+    ("w64_two_chunks_no_meta", "bf16", 1, 2, 128, 128, 64, 0, 3.0, 1.0, 0.7),
+    ("w64_ragged_max_meta", "bf16", 1, 2, 333, 128, 64, 16, 0.0, 2.0, 1.0),
     # head dim 64 on the tensor-core pipeline (tiles zero-padded to 128)
     ("d64_window_one", "bf16", 1, 2, 150, 64, 1, 3, 3.0, 1.0, 1.0),
     ("d64_window_65", "bf16", 1, 2, 333, 64, 65, 4, 3.0, 1.0, 1.0),
