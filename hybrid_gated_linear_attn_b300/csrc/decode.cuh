@@ -46,7 +46,13 @@ struct DecodeArgs {
 };
 
 constexpr int DECODE_THREADS = 256;
-constexpr int DECODE_SPLIT = 2;        // CTAs per unit (value-column halves)
+// CTAs per unit (value-column slices): two at d <= 128, eight at d = 256, so
+// that a CTA's slice of S stays 32 registers a thread.
+template <int D>
+__host__ __device__ constexpr int decode_split()
+{
+    return D > 128 ? 8 : 2;
+}
 constexpr int DECODE_KEY_THREADS = 8;  // threads per window key in the logit pass
 constexpr uint32_t DECODE_WAIT_LIMIT = 1u << 22;
 constexpr unsigned long long DECODE_POS_TICK = 1ull << 40;  // per-CTA arrival count in pos's high bits
@@ -61,7 +67,7 @@ struct DecodePlan {
 template <int D>
 __host__ __device__ inline DecodePlan decode_plan(int esize, int w, int m)
 {
-    constexpr int RG = DECODE_THREADS / (D / DECODE_SPLIT / 4);
+    constexpr int RG = DECODE_THREADS / (D / decode_split<D>() / 4);
     DecodePlan p;
     p.ring_bytes = (size_t)w * D * esize;
     p.tok_bytes = (size_t)D * esize;                  // one of q, k, v, g
@@ -70,9 +76,9 @@ __host__ __device__ inline DecodePlan decode_plan(int esize, int w, int m)
     // ring keys | ring values | q | k | v | g | meta keys of the unit's head
     p.copy_bytes = 2 * p.ring_bytes + 4 * p.tok_bytes + p.mu_bytes;
     // then: q, k, v, gamma as fp32 [D]; logits [w + m] (rounded to 4);
-    // row-group partials [RG][D / 2]; stats [4]; two mbarriers (the token
-    // and meta-key copies, the ring copies).
-    p.total = p.copy_bytes + 4 * ((size_t)4 * D + ((w + m + 3) / 4) * 4 + (size_t)RG * (D / DECODE_SPLIT) + 4) + 16;
+    // row-group partials [RG][D / split]; stats [4]; two mbarriers (the
+    // token and meta-key copies, the ring copies).
+    p.total = p.copy_bytes + 4 * ((size_t)4 * D + ((w + m + 3) / 4) * 4 + (size_t)RG * (D / decode_split<D>()) + 4) + 16;
     return p;
 }
 
@@ -120,12 +126,13 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8])
     }
 }
 
-// grid = DECODE_SPLIT * B * H; CTA (unit, half) owns value columns
-// [half * D/2, half * D/2 + D/2).
+// grid = split * B * H; CTA (unit, slice) owns value columns
+// [slice * D/split, (slice + 1) * D/split).
 template <typename T, int D>
 __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeArgs a)
 {
-    constexpr int DH = D / DECODE_SPLIT;             // value columns of this CTA
+    constexpr int SPLIT = decode_split<D>();
+    constexpr int DH = D / SPLIT;                    // value columns of this CTA
     constexpr int CQ = DH / 4;                       // column quads per row of S
     constexpr int RG = DECODE_THREADS / CQ;          // row groups
     constexpr int RPT = D / RG;                      // rows of S per thread
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
     static_assert(RG * CQ == DECODE_THREADS && RPT * RG == D && DPT % 8 == 0, "decode tiling");
 
     const int w = a.w, m = a.m, H = a.H;
-    const int u = blockIdx.x / DECODE_SPLIT, half = blockIdx.x % DECODE_SPLIT, j0 = half * DH;
+    const int u = blockIdx.x / SPLIT, half = blockIdx.x % SPLIT, j0 = half * DH;
     const int b = u / H;
     const DecodePlan plan = decode_plan<D>((int)sizeof(T), w, m);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -190,9 +197,9 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
 #pragma unroll
     for (int r = 0; r < RPT; ++r) s_reg[r] = Sg[(size_t)(rg + r * RG) * (D / 4) + cq];
     // The position, read and advanced in one pass without a second kernel:
-    // each of the 2H CTAs of sequence b adds 2^40 to pos[b] and takes the
+    // each of the split x H CTAs of sequence b adds 2^40 to pos[b] and takes the
     // token count from the low 40 bits of the value it got back; the CTA
-    // whose addition was the last (2H - 1 earlier ones) writes p + 1.  So
+    // whose addition was the last (split x H - 1 earlier ones) writes p + 1.  So
     // every CTA sees the same p whatever the scheduling order, and pos[b]
     // is p + 1 once the kernel is done.
     __shared__ long long p_sh;
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
         const unsigned long long old =
             atomicAdd(reinterpret_cast<unsigned long long *>(const_cast<int64_t *>(a.pos) + b), DECODE_POS_TICK);
         const long long cnt = (long long)old >> 40, pv = (long long)(old & (DECODE_POS_TICK - 1));
-        const int ctas = DECODE_SPLIT * H;
+        const int ctas = SPLIT * H;
         if (cnt < 0 || cnt >= ctas) {
             p_sh = -1;  // pos[b] was outside [0, 2^40) before the call
         } else {

@@ -107,7 +107,7 @@ static lizard_status check_state(const lizard_state *st)
     // a slice of the batch (pos + b0) is a valid state too
     if (!aligned16(st->S) || !aligned16(st->ring_k) || !aligned16(st->ring_v) || !aligned8(st->pos))
         return LIZARD_ERR_INVALID_ARG;
-    if (st->dk != st->dv || (st->dk != 64 && st->dk != 128)) return LIZARD_ERR_UNSUPPORTED;
+    if (st->dk != st->dv || (st->dk != 64 && st->dk != 128 && st->dk != 256)) return LIZARD_ERR_UNSUPPORTED;
     if (st->w > LIZARD_MAX_WINDOW) return LIZARD_ERR_UNSUPPORTED;
     return LIZARD_OK;
 }
@@ -124,7 +124,14 @@ static lizard_status launch_prefill(const PrefillArgs &pa, cudaStream_t s)
     auto kern = prefill_simt_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    kern<<<pa.B * pa.H, SIMT_THREADS, smem, s>>>(pa);
+    constexpr int NSL = SimtShape<D>::NSL;
+    kern<<<pa.B * pa.H * NSL, SIMT_THREADS, smem, s>>>(pa);
+    if constexpr (NSL > 1) {
+        if (pa.S_out) {
+            if (launch_status() != LIZARD_OK) return LIZARD_ERR_CUDA;
+            ring_handoff_kernel<T, D><<<pa.B * pa.H, SIMT_THREADS, 0, s>>>(pa);
+        }
+    }
     return launch_status();
 }
 
@@ -332,7 +339,7 @@ static lizard_status launch_decode(DecodeArgs da, cudaStream_t s)
     // previous kernel on the stream drains; the kernel waits for it
     // (griddepcontrol.wait) before touching any data.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(da.B * da.H * DECODE_SPLIT));
+    cfg.gridDim = dim3((unsigned)(da.B * da.H * decode_split<D>()));
     cfg.blockDim = dim3(DECODE_THREADS);
     cfg.dynamicSmemBytes = plan.total;
     cfg.stream = s;
@@ -625,7 +632,7 @@ lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v,
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(y) ||
         (m > 0 && !aligned16(meta_k)))
         return LIZARD_ERR_INVALID_ARG;
-    if (dk != dv || (dk != 64 && dk != 128)) return LIZARD_ERR_UNSUPPORTED;
+    if (dk != dv || (dk != 64 && dk != 128 && dk != 256)) return LIZARD_ERR_UNSUPPORTED;
     if (w > LIZARD_MAX_WINDOW || m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
     if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
     if (st) {
@@ -640,6 +647,8 @@ lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v,
                    st ? st->S : nullptr, st ? st->ring_k : nullptr, st ? st->ring_v : nullptr,
                    st ? st->pos : nullptr, 0, nullptr, alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
+    if (dk == 256)  // CUDA cores, value slices
+        return dtype == LIZARD_BF16 ? launch_prefill<__nv_bfloat16, 256>(pa, s) : launch_prefill<float, 256>(pa, s);
     if (dtype == LIZARD_BF16)
         return dk == 128 ? launch_prefill_ws(pa, s)
                          : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
@@ -714,6 +723,8 @@ lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const
     PrefillArgs pa{q, k, v, g, meta_k, y, alpha, B, H, L, w, m, st->S, st->ring_k, st->ring_v, st->pos, 1, st->S,
                    alpha_h, group};
     cudaStream_t s = (cudaStream_t)stream;
+    if (dk == 256)  // CUDA cores, value slices
+        return st->dtype == LIZARD_BF16 ? launch_prefill<__nv_bfloat16, 256>(pa, s) : launch_prefill<float, 256>(pa, s);
     if (st->dtype == LIZARD_BF16)
         return dk == 128 ? launch_prefill_ws(pa, s)
                          : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
@@ -818,13 +829,20 @@ lizard_status lizard_attn_decode_step_v(const void *q, const void *k, const void
         (m > 0 && !aligned16(meta_k)))
         return LIZARD_ERR_INVALID_ARG;
     if (m > LIZARD_MAX_META) return LIZARD_ERR_UNSUPPORTED;
+    // The CTAs of one sequence (up to 8 H) count their arrivals in pos's
+    // high bits, which hold counts below 2^23.
+    if (st->H >= (1 << 20)) return LIZARD_ERR_UNSUPPORTED;
     if (st->B == 0) return LIZARD_OK;
     DecodeArgs da{q, k, v, g, meta_k, y, st->S, st->ring_k, st->ring_v, st->pos, alpha, st->B, st->H, st->w, m,
                   alpha_h, group, -1};
     cudaStream_t s = (cudaStream_t)stream;
     if (st->dtype == LIZARD_BF16)
-        return st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s) : launch_decode<__nv_bfloat16, 64>(da, s);
-    return st->dk == 128 ? launch_decode<float, 128>(da, s) : launch_decode<float, 64>(da, s);
+        return st->dk == 256   ? launch_decode<__nv_bfloat16, 256>(da, s)
+               : st->dk == 128 ? launch_decode<__nv_bfloat16, 128>(da, s)
+                               : launch_decode<__nv_bfloat16, 64>(da, s);
+    return st->dk == 256 ? launch_decode<float, 256>(da, s)
+           : st->dk == 128 ? launch_decode<float, 128>(da, s)
+                           : launch_decode<float, 64>(da, s);
 }
 
 lizard_status lizard_scratch_trim(size_t keep_bytes)

@@ -41,8 +41,13 @@
  *     so far, e.g. about 810 MB for the backward of B4 H32 L4096 d128 --
  *     until lizard_scratch_trim returns it or the process exits; failure to
  *     allocate is LIZARD_ERR_CUDA (a prefill then runs unsegmented instead).
- *   - Supported shapes: d_k == d_v in {64, 128}; 1 <= w <= LIZARD_MAX_WINDOW;
- *     0 <= m <= LIZARD_MAX_META.  Anything else in range but not built is
+ *   - Supported shapes: d_k == d_v in {64, 128, 256}; 1 <= w <= LIZARD_MAX_WINDOW;
+ *     0 <= m <= LIZARD_MAX_META.  d = 256 runs the exact CUDA-core kernels
+ *     (prefill, continued prefill, decode; its backward is not built: the
+ *     backward and the no-allocation prefill take d in {64, 128}); a decode
+ *     step at d = 256 in fp32 stages its ring and meta keys in shared
+ *     memory and is UNSUPPORTED where they do not fit (w > 99 with 16 meta
+ *     keys, w > 107 with none).  Anything else in range but not built is
  *     LIZARD_ERR_UNSUPPORTED; anything meaningless is LIZARD_ERR_INVALID_ARG.
  */
 #ifndef LIZARD_ATTN_H

@@ -68,7 +68,7 @@ def state(S=A, rk=A, rv=A, pos=A, Bn=2, H=4, dk=128, dv=128, w=64, dtype=LA.LIZA
     (dict(q=MIS), INVALID), (dict(y=MIS), INVALID), (dict(mu=MIS), INVALID),
     (dict(dtype=7), INVALID), (dict(w=0), INVALID), (dict(w=-3), INVALID), (dict(m=-1), INVALID),
     (dict(L=-1), INVALID), (dict(H=0), INVALID), (dict(Bn=-1), INVALID), (dict(dk=0), INVALID),
-    (dict(dk=96, dv=96), UNSUPPORTED), (dict(dk=128, dv=64), UNSUPPORTED), (dict(dk=256, dv=256), UNSUPPORTED),
+    (dict(dk=96, dv=96), UNSUPPORTED), (dict(dk=128, dv=64), UNSUPPORTED), (dict(dk=512, dv=512), UNSUPPORTED),
     (dict(w=LA.LIZARD_MAX_WINDOW + 1), UNSUPPORTED), (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
 ])
 def test_prefill_rejects(lib, kw, code):
@@ -117,6 +117,10 @@ def decode(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, m=4, y=A, st="default"):
     (dict(st=state(w=0)), INVALID), (dict(st=state(H=0)), INVALID), (dict(st=state(dtype=5)), INVALID),
     (dict(st=state(dk=96, dv=96)), UNSUPPORTED), (dict(st=state(w=LA.LIZARD_MAX_WINDOW + 1)), UNSUPPORTED),
     (dict(st=state(S=None)), INVALID), (dict(st=state(rk=MIS)), INVALID),
+    # d = 256 in fp32 stages ring and meta keys in shared memory: w = 100 with
+    # 16 meta keys does not fit (checked on the host, before any launch)
+    (dict(st=state(dk=256, dv=256, w=100, dtype=LA.LIZARD_F32), m=16), UNSUPPORTED),
+    (dict(st=state(H=1 << 20)), UNSUPPORTED),
 ])
 def test_decode_rejects(lib, kw, code):
     assert decode(lib, **kw) == code
@@ -175,6 +179,7 @@ def backward(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128,
     (dict(dal=A + 2), INVALID), (dict(dy=MIS), INVALID), (dict(dmu=MIS), INVALID),
     (dict(dtype=7), INVALID), (dict(w=0), INVALID), (dict(m=-1), INVALID), (dict(L=-1), INVALID),
     (dict(H=0), INVALID), (dict(dk=96, dv=96), UNSUPPORTED), (dict(dk=128, dv=64), UNSUPPORTED),
+    (dict(dk=256, dv=256), UNSUPPORTED),  # the backward is built for d in {64, 128}
     (dict(w=LA.LIZARD_MAX_WINDOW + 1), UNSUPPORTED), (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
 ])
 def test_backward_rejects(lib, kw, code):
@@ -238,7 +243,7 @@ def noalloc(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128, 
     # or d = 64 with w <= 65
     (dict(dtype=LA.LIZARD_F32), UNSUPPORTED), (dict(dk=64, dv=64, w=66), UNSUPPORTED),
     (dict(dk=64, dv=128), UNSUPPORTED), (dict(dk=96, dv=96), UNSUPPORTED), (dict(w=129), UNSUPPORTED),
-    (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED),
+    (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED), (dict(dk=256, dv=256, st=state(dk=256, dv=256)), UNSUPPORTED),
     (dict(q=None), INVALID), (dict(g=None), INVALID), (dict(y=None), INVALID), (dict(mu=None), INVALID),
     (dict(v=MIS), INVALID), (dict(y=MIS), INVALID), (dict(dtype=7), INVALID), (dict(w=0), INVALID),
     (dict(m=-1), INVALID), (dict(L=-1), INVALID), (dict(H=0), INVALID), (dict(Bn=-1), INVALID),

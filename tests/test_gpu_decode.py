@@ -56,6 +56,8 @@ def _run_decode(wl, steps, seq=None):
     (64, 16, 0, 40, "f32"),       # no sinks
     (64, 1, 3, 5, "f32"),         # window of one token
     (128, 128, 16, 300, "bf16"),  # largest window and meta count
+    (256, 64, 4, 70, "bf16"),     # head dim 256: eight value slices per unit
+    (256, 96, 16, 20, "f32"),     # head dim 256 in fp32, ring still filling
 ])
 def test_decode_small(d, w, m, hist, dtype):
     wl = WORKLOADS["decode"].replace(B=3, H=4, dk=d, dv=d, w=w, m=m, L=hist, dtype=dtype)

@@ -100,6 +100,12 @@ CASES = [
     ("d64_long_prompt_few_units", "bf16", 1, 2, 3000, 64, 64, 4, 3.0, 1.0, 0.7),
     ("d64_more_units_than_sms", "bf16", 5, 32, 70, 64, 64, 4, 3.0, 1.0, 1.0),
     ("d64_w100_cuda_cores", "bf16", 1, 2, 300, 64, 100, 4, 3.0, 1.0, 1.0),
+    # head dim 256 on the CUDA cores (four value slices per unit, 32-token chunks)
+    ("d256_bf16_ragged", "bf16", 2, 2, 150, 256, 64, 4, 3.0, 1.0, 1.0),
+    ("d256_f32_w128_max_meta", "f32", 1, 2, 170, 256, 128, 16, 0.0, 2.0, 0.5),
+    ("d256_f32_window_one", "f32", 1, 2, 70, 256, 1, 2, 3.0, 1.0, 0.7),
+    ("d256_bf16_single_token", "bf16", 2, 2, 1, 256, 48, 4, 3.0, 1.0, 1.0),
+    ("d256_bf16_strong_decay_no_meta", "bf16", 1, 3, 100, 256, 33, 0, -6.0, 3.0, 1.0),
 ]
 
 
