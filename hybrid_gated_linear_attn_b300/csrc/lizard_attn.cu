@@ -210,16 +210,43 @@ static int prefill_segments(int units, int nchunks)
     return p < 1 || cap < 1 ? 1 : (p < cap ? p : cap);
 }
 
-// Bytes of scratch a segmented prefill needs: the segment states and decays,
-// and for a continued prompt copies of its start state and window history.
-static size_t segment_states_bytes(int units, int nseg)
+// Scratch of a segmented prefill, in order: the segments' start states
+// [units][nseg-1][D][D] (what the prefill reads); with sub-blocks (nsub > 1)
+// the sub-blocks' end states [units][(nseg-1) nsub][D][D] (with nsub = 1
+// they share the start states' space: the scan writes each over what it
+// has just read); the decays [units][(nseg-1) nsub][D]; for a continued
+// prompt copies of its start state and window history.  All fp32 but the
+// history (bf16); every offset a multiple of 16 bytes.
+struct SegLayout {
+    size_t sub_off, lam_off, cont_off, total;
+};
+static SegLayout segment_layout(int units, int nseg, int nsub, bool cont)
 {
-    return (size_t)units * (nseg - 1) * ((size_t)ws::D * ws::D + ws::D) * sizeof(float);
+    const size_t DD = (size_t)ws::D * ws::D * sizeof(float), nsp = (size_t)units * (nseg - 1);
+    SegLayout l;
+    l.sub_off = nsub > 1 ? nsp * DD : 0;
+    l.lam_off = nsp * DD + (nsub > 1 ? nsp * nsub * DD : 0);
+    l.cont_off = l.lam_off + nsp * nsub * ws::D * sizeof(float);
+    l.total = l.cont_off + (cont ? (size_t)units * (DD + 2 * ws::C * ws::D * sizeof(__nv_bfloat16)) : 0);
+    return l;
 }
-static size_t segment_scratch_bytes(int units, int nseg, bool cont = false)
+
+// Sub-blocks per segment in the pre-pass: the count (1..8) whose CTAs, in
+// whole waves over the SMs (one pre-pass CTA per SM), walk the fewest chunks
+// one after another; ties go to fewer sub-blocks.
+static int segment_subblocks(int units, int nseg, int seg_chunks)
 {
-    return segment_states_bytes(units, nseg) +
-           (cont ? (size_t)units * (ws::D * ws::D * sizeof(float) + 2 * ws::C * ws::D * sizeof(__nv_bfloat16)) : 0);
+    const long long sms = sm_count(), ctas = (long long)units * (nseg - 1);
+    int best = 1;
+    long long best_cost = -1;
+    for (int nsub = 1; nsub <= 8 && nsub <= seg_chunks; ++nsub) {
+        const long long cost = ((ctas * nsub + sms - 1) / sms) * ((seg_chunks + nsub - 1) / nsub);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = nsub;
+        }
+    }
+    return best;
 }
 
 // The segment pre-pass: end state and total decay of every segment but the
@@ -227,16 +254,20 @@ static size_t segment_scratch_bytes(int units, int nseg, bool cont = false)
 // For a continued prompt `sc` names its start state and the copies the
 // first segment reads.
 static lizard_status launch_segment_states(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tg,
-                                           float *scratch, int units, int L, int seg_chunks, int nseg,
-                                           const seg::ScanCont &sc, int H, int group, cudaStream_t s)
+                                           float *scratch, const SegLayout &lay, int nsub, int units, int L,
+                                           int seg_chunks, int nseg, const seg::ScanCont &sc, int H, int group,
+                                           cudaStream_t s)
 {
-    seg::SegArgs sa{scratch, scratch + (size_t)units * (nseg - 1) * ws::D * ws::D, L, seg_chunks, nseg, H, group};
+    uint8_t *base = reinterpret_cast<uint8_t *>(scratch);
+    seg::SegArgs sa{reinterpret_cast<float *>(base + lay.sub_off), reinterpret_cast<float *>(base + lay.lam_off),
+                    L, seg_chunks, nseg, H, group, nsub, (seg_chunks + nsub - 1) / nsub};
     if (cudaFuncSetAttribute(seg::segment_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)seg::SMEM_BYTES) != cudaSuccess)
         return LIZARD_ERR_CUDA;
-    seg::segment_state_kernel<<<units * (nseg - 1), seg::THREADS, seg::SMEM_BYTES, s>>>(tk, tv, tg, sa);
+    seg::segment_state_kernel<<<units * (nseg - 1) * nsub, seg::THREADS, seg::SMEM_BYTES, s>>>(tk, tv, tg, sa);
     if (cudaGetLastError() != cudaSuccess) return LIZARD_ERR_CUDA;
-    seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, units, nseg, sc);
+    seg::segment_scan_kernel<<<dim3(ws::D * ws::D / 256, units), 256, 0, s>>>(sa.dS, sa.lam, scratch, units, nseg,
+                                                                              nsub, sc);
     return launch_status();
 }
 
@@ -266,9 +297,17 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
         !make_token_map(&tv, pa.v, kv_units, pa.L, d) || !make_token_map(&tg, pa.g, units, pa.L, d))
         return LIZARD_ERR_CUDA;
     float *seg_states = nullptr;
+    int nsub = 1;
+    SegLayout lay{};
     bool owned = false;
     if (nseg > 1) {
-        const size_t need = segment_scratch_bytes(units, nseg, pa.cont != 0);
+        nsub = segment_subblocks(units, nseg, seg_chunks);
+        lay = segment_layout(units, nseg, nsub, pa.cont != 0);
+        if (scratch && scratch_bytes < lay.total) {  // the allocation-free call's fixed array: whole segments
+            nsub = 1;
+            lay = segment_layout(units, nseg, nsub, pa.cont != 0);
+        }
+        const size_t need = lay.total;
         if (scratch) {
             if (scratch_bytes < need) return LIZARD_ERR_UNSUPPORTED;
             seg_states = scratch;
@@ -288,15 +327,15 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
     if (nseg > 1) {
         seg::ScanCont sc{};
         if (pa.cont) {
-            float *copy = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(seg_states) +
-                                                    segment_states_bytes(units, nseg));
+            float *copy = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(seg_states) + lay.cont_off);
             __nv_bfloat16 *hcopy = reinterpret_cast<__nv_bfloat16 *>(copy + (size_t)units * ws::D * ws::D);
             sc = seg::ScanCont{pa.S0, copy, static_cast<const __nv_bfloat16 *>(pa.ring_k),
                                static_cast<const __nv_bfloat16 *>(pa.ring_v), pa.pos, hcopy, pa.H, pa.w};
             seg0_state = copy;
             hist = hcopy;
         }
-        rc = launch_segment_states(tk, tv, tg, seg_states, units, pa.L, seg_chunks, nseg, sc, pa.H, pa.group, s);
+        rc = launch_segment_states(tk, tv, tg, seg_states, lay, nsub, units, pa.L, seg_chunks, nseg, sc, pa.H,
+                                   pa.group, s);
     }
     ws::WsArgs wa{static_cast<const __nv_bfloat16 *>(pa.g), static_cast<const __nv_bfloat16 *>(pa.mu),
                   static_cast<const __nv_bfloat16 *>(pa.k), static_cast<const __nv_bfloat16 *>(pa.v),

@@ -50,14 +50,19 @@ constexpr uint32_t OFF_FLAG = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_TSLOT = OFF_FLAG + 16;
 constexpr uint32_t SMEM_BYTES = OFF_TSLOT + 16 + 1024;
 
+// Every segment but the last is walked as nsub sub-blocks of sub_chunks
+// chunks (the walk is latency-bound: more, shorter walks side by side).
 struct SegArgs {
-    float *dS;      // [units][nseg-1][D][D] fp32, row = key dim
-    float *lam;     // [units][nseg-1][D] fp32 (base-2 log of the segment's decay)
+    float *dS;      // [units][(nseg-1) nsub][D][D] fp32, row = key dim
+    float *lam;     // [units][(nseg-1) nsub][D] fp32 (base-2 log of the sub-block's decay)
     int L, seg_chunks, nseg;
     int H, group;   // query heads per key/value head (tk, tv map B x H / group heads)
+    int nsub, sub_chunks;
 };
 
-// grid = units * (nseg - 1): CTA (unit, p) covers chunks [p * seg_chunks, (p+1) * seg_chunks).
+// grid = units * (nseg - 1) * nsub: CTA (unit, q), q = p nsub + b, covers
+// sub-block b of segment p: chunks [p seg_chunks + b sub_chunks, ...), at
+// most sub_chunks of them and none past the segment.
 __global__ void __launch_bounds__(THREADS, 1)
     segment_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap tg, const SegArgs a)
@@ -73,10 +78,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TSLOT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nsp = a.nseg - 1;
+    const int nsp = (a.nseg - 1) * a.nsub;  // sub-blocks per unit
     const int unit = blockIdx.x / nsp, p = blockIdx.x % nsp;
+    const int seg = p / a.nsub, sb_i = p % a.nsub;
     const int nchunks_all = (a.L + C - 1) / C;
-    const int c_begin = p * a.seg_chunks, c_end = min(nchunks_all, c_begin + a.seg_chunks);
+    const int seg_end = min(nchunks_all, (seg + 1) * a.seg_chunks);
+    const int c_begin = seg * a.seg_chunks + sb_i * a.sub_chunks, c_end = min(seg_end, c_begin + a.sub_chunks);
     const int nch = max(0, c_end - c_begin);
 
     if (warp == W_MMA) {
@@ -255,16 +262,19 @@ struct ScanCont {
     int H, w;
 };
 
-// Segment start states: S_start(0) = S0 (zero when S0 is null) and
-// S_start(p+1) = diag(2^{Lam_p}) S_start(p) + dS_p, written over dS_p, so
-// that dS[u][p] holds S_start(p + 1) afterwards.  For a continued prompt
+// Segment start states: S_start(0) = S0 (zero when S0 is null), the state
+// folded through the sub-blocks in order, S <- diag(2^{Lam_q}) S + dS_q, and
+// after the last sub-block of segment p written to Sst[u][p] = S_start(p + 1)
+// (Sst may be dS itself when nsub = 1: each element is read before it is
+// written, by the same thread).  For a continued prompt
 // the first segment's inputs are copied as well: S0, and the window history
 // (row r = token r - C, from ring slot (p0 + r - C) % w with p0 = the low 40
 // bits of pos, as the prefill takes it; zero rows where no key).  One
 // thread per state element and unit.
-__global__ void segment_scan_kernel(float *dS, const float *lam, int units, int nseg, ScanCont sc)
+__global__ void segment_scan_kernel(float *dS, const float *lam, float *Sst, int units, int nseg, int nsub,
+                                    ScanCont sc)
 {
-    const int nsp = nseg - 1;
+    const int nsp = nseg - 1, nq = nsp * nsub;
     const int u = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;  // i * D + j
     if (u >= units || e >= D * D) return;
@@ -281,10 +291,10 @@ __global__ void segment_scan_kernel(float *dS, const float *lam, int units, int 
     const int i = e / D;
     float S = sc.S0 ? sc.S0[(size_t)u * D * D + e] : 0.f;
     if (sc.S0_copy) sc.S0_copy[(size_t)u * D * D + e] = S;
-    for (int q = 0; q < nsp; ++q) {
-        const size_t off = ((size_t)u * nsp + q) * D * D + e;
-        S = exp2f(lam[((size_t)u * nsp + q) * D + i]) * S + dS[off];
-        dS[off] = S;
+    for (int q = 0; q < nq; ++q) {
+        const size_t off = ((size_t)u * nq + q) * D * D + e;
+        S = exp2f(lam[((size_t)u * nq + q) * D + i]) * S + dS[off];
+        if ((q + 1) % nsub == 0) Sst[((size_t)u * nsp + q / nsub) * D * D + e] = S;
     }
 }
 
