@@ -40,15 +40,17 @@ constexpr int OUT_N = 128, PREP_N = 256;
 enum : int { NB_OUT_R = 1, NB_PREP = 2, NB_PREP_R = 3 };
 constexpr int ST = 2;  // stages
 
-// Shared memory: per stage g | k | v (16 KiB each), then two scaled-key tiles.
+// Shared memory: per stage g | k | v (16 KiB each), then one scaled-key
+// tile per stage.
 constexpr uint32_t STAGE = 3 * 2 * KB_T;
 constexpr uint32_t OFF_KH = ST * STAGE;
-constexpr uint32_t OFF_TOT = OFF_KH + 2 * 2 * KB_T;   // [4][128] fp32 quarter totals
+constexpr uint32_t OFF_TOT = OFF_KH + ST * 2 * KB_T;  // [4][128] fp32 quarter totals
 constexpr uint32_t OFF_BAR = OFF_TOT + 4 * 128 * 4;
 constexpr int NBAR = 4 * ST + 2;
 constexpr uint32_t OFF_FLAG = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_TSLOT = OFF_FLAG + 16;
 constexpr uint32_t SMEM_BYTES = OFF_TSLOT + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Every segment but the last is walked as nsub sub-blocks of sub_chunks
 // chunks (the walk is latency-bound: more, shorter walks side by side).
