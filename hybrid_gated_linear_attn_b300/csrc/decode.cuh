@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
     float *k_s = q_s + D, *v_s = k_s + D, *gam_s = v_s + D;
     float *sc = gam_s + D;                      // [w + m] logits
     float *red = sc + ((w + m + 3) / 4) * 4;    // [RG][DH]
-    float *stat = red + RG * DH;                // M, alpha / Z
+    float *stat = red + RG * DH;                // [1]: alpha / Z
     uint64_t *bar = reinterpret_cast<uint64_t *>(stat + 4);
 
     // The next decode step may begin launching now; this one waits until the
@@ -322,26 +322,29 @@ __global__ void __launch_bounds__(DECODE_THREADS, 4) decode_step_kernel(DecodeAr
     }
     __syncthreads();
 
-    // 5. Softmax statistics over the window and the sinks.
+    // 5. Softmax statistics over the window and the sinks; each logit is
+    //    replaced by its exponential e^{s - M}, so that the anchor sum below
+    //    takes every key's once instead of once per thread that uses it.
     if (warp == 0) {
         float M = -INFINITY;
         for (int c = lane; c < n + m; c += 32) M = fmaxf(M, sc[c]);
         M = warp_max(M);
         float Z = 0.f;
-        for (int c = lane; c < n + m; c += 32) Z += expf(sc[c] - M);
-        Z = warp_sum(Z);
-        if (lane == 0) {
-            stat[0] = M;
-            stat[1] = head_alpha(a.alpha_h, a.alpha, u % H) / Z;
+        for (int c = lane; c < n + m; c += 32) {
+            const float e = expf(sc[c] - M);
+            sc[c] = e;
+            Z += e;
         }
+        Z = warp_sum(Z);
+        if (lane == 0) stat[1] = head_alpha(a.alpha_h, a.alpha, u % H) / Z;
     }
     __syncthreads();
-    const float M = stat[0], scale = stat[1];
+    const float scale = stat[1];
 
     // 6. Anchor partial: this row group's share of the window keys, for this
     //    CTA's columns.
     for (int c = rg; c < n; c += RG) {
-        const float pc = expf(sc[c] - M) * scale;
+        const float pc = sc[c] * scale;
         const float4 vv = c < nh ? load4(rv + (size_t)((first + c) % w) * D + j0 + cq * 4)
                                  : *reinterpret_cast<const float4 *>(v_s + j0 + cq * 4);
         acc.x += pc * vv.x;
