@@ -311,8 +311,10 @@ LIZARD_API lizard_status lizard_gate_projection(const void *x, const void *w_gam
  * At p = pos[b]: S <- diag(sigmoid(g)) S + k^T v; yg = q S; the window is the
  * current token plus tokens max(0, p-w+1) .. p-1 read from the ring; then
  * the current k, v go to ring slot p % w and pos[b] becomes p + 1.
- * Enqueues one kernel.  Precondition: 0 <= pos[b] < 2^40 (a state written
- * by this library always is).  While the kernel runs, pos[b] carries an
+ * Enqueues one kernel.  st->H < 2^20 (LIZARD_ERR_UNSUPPORTED otherwise:
+ * the CTAs of a sequence count their arrivals in pos's high bits).
+ * Precondition: 0 <= pos[b] < 2^40 (a state written by this library always
+ * is).  While the kernel runs, pos[b] carries an
  * arrival count in its high bits; it holds p + 1 again once the step is
  * done.  A pos outside that range is reported (see
  * lizard_check_device_status); that sequence's y, S, ring and pos are then
