@@ -347,8 +347,9 @@ static lizard_status launch_prefill_ws(const PrefillArgs &pa, cudaStream_t s, fl
         rc = d == ws::D ? (pa.w == 1   ? launch_prefill_ws_np<0, ws::D>(tq, tk, tv, wa, units * nseg, s)
                            : pa.w <= 65 ? launch_prefill_ws_np<1, ws::D>(tq, tk, tv, wa, units * nseg, s)
                                         : launch_prefill_ws_np<2, ws::D>(tq, tk, tv, wa, units * nseg, s))
-                        : (pa.w == 1 ? launch_prefill_ws_np<0, 64>(tq, tk, tv, wa, units * nseg, s)
-                                     : launch_prefill_ws_np<1, 64>(tq, tk, tv, wa, units * nseg, s));
+                        : (pa.w == 1   ? launch_prefill_ws_np<0, 64>(tq, tk, tv, wa, units * nseg, s)
+                           : pa.w <= 65 ? launch_prefill_ws_np<1, 64>(tq, tk, tv, wa, units * nseg, s)
+                                        : launch_prefill_ws_np<2, 64>(tq, tk, tv, wa, units * nseg, s));
     if (owned && cudaFreeAsync(seg_states, s) != cudaSuccess && rc == LIZARD_OK) rc = LIZARD_ERR_CUDA;
     return rc;
 }
@@ -690,7 +691,7 @@ lizard_status lizard_attn_prefill_v(const void *q, const void *k, const void *v,
         return dtype == LIZARD_BF16 ? launch_prefill<__nv_bfloat16, 256>(pa, s) : launch_prefill<float, 256>(pa, s);
     if (dtype == LIZARD_BF16)
         return dk == 128 ? launch_prefill_ws(pa, s)
-                         : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
+                         : launch_prefill_ws(pa, s, nullptr, 0, 0, 64);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 
@@ -707,7 +708,7 @@ lizard_status lizard_attn_prefill_noalloc(const void *q, const void *k, const vo
         (m > 0 && !aligned16(meta_k)))
         return LIZARD_ERR_INVALID_ARG;
     // The variant covers the tensor-core prefill, the one with scratch.
-    if (dtype != LIZARD_BF16 || dk != dv || !((dk == 128 && w <= LIZARD_MAX_WINDOW) || (dk == 64 && w <= 65)) ||
+    if (dtype != LIZARD_BF16 || dk != dv || !(dk == 128 || dk == 64) || w > LIZARD_MAX_WINDOW ||
         m > LIZARD_MAX_META)
         return LIZARD_ERR_UNSUPPORTED;
     if ((int64_t)B * H > 2147483647LL || (int64_t)L * dk > (int64_t)1 << 40) return LIZARD_ERR_UNSUPPORTED;
@@ -766,7 +767,7 @@ lizard_status lizard_attn_prefill_continue_v(const void *q, const void *k, const
         return st->dtype == LIZARD_BF16 ? launch_prefill<__nv_bfloat16, 256>(pa, s) : launch_prefill<float, 256>(pa, s);
     if (st->dtype == LIZARD_BF16)
         return dk == 128 ? launch_prefill_ws(pa, s)
-                         : (w <= 65 ? launch_prefill_ws(pa, s, nullptr, 0, 0, 64) : launch_prefill<__nv_bfloat16, 64>(pa, s));
+                         : launch_prefill_ws(pa, s, nullptr, 0, 0, 64);
     return dk == 128 ? launch_prefill<float, 128>(pa, s) : launch_prefill<float, 64>(pa, s);
 }
 

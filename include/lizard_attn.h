@@ -209,8 +209,8 @@ LIZARD_API lizard_status lizard_attn_prefill_continue_v(const void *q, const voi
  * no counterpart; this entry point is about memory management only.)
  *
  * Same arguments and results as lizard_attn_prefill; it covers the
- * tensor-core path (bf16 with dk == dv == 128, or dk == dv == 64 and
- * w <= 65), LIZARD_ERR_UNSUPPORTED otherwise.  When a prompt runs as sequence segments (few batch x head
+ * tensor-core path (bf16 with dk == dv in {64, 128}), LIZARD_ERR_UNSUPPORTED
+ * otherwise.  When a prompt runs as sequence segments (few batch x head
  * units, long L) the segments' start states need scratch.  This variant
  * keeps it in a fixed device array of LIZARD_NOALLOC_SCRATCH_BYTES (16 MiB)
  * that every GPU loading the library holds until the process exits, and

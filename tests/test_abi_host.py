@@ -239,9 +239,8 @@ def noalloc(lib, q=A, k=A, v=A, g=A, mu=A, alpha=1.0, Bn=2, H=4, L=128, dk=128, 
 
 
 @pytest.mark.parametrize("kw,code", [
-    # the allocation-free call covers the bf16 tensor-core prefill only: d = 128,
-    # or d = 64 with w <= 65
-    (dict(dtype=LA.LIZARD_F32), UNSUPPORTED), (dict(dk=64, dv=64, w=66), UNSUPPORTED),
+    # the allocation-free call covers the bf16 tensor-core prefill only: d = 128 or 64
+    (dict(dtype=LA.LIZARD_F32), UNSUPPORTED),
     (dict(dk=64, dv=128), UNSUPPORTED), (dict(dk=96, dv=96), UNSUPPORTED), (dict(w=129), UNSUPPORTED),
     (dict(m=LA.LIZARD_MAX_META + 1), UNSUPPORTED), (dict(dk=256, dv=256, st=state(dk=256, dv=256)), UNSUPPORTED),
     (dict(q=None), INVALID), (dict(g=None), INVALID), (dict(y=None), INVALID), (dict(mu=None), INVALID),

@@ -93,7 +93,7 @@ CASES = [
     # CUDA-core path (fp32, or bf16 d = 64 with w > 65)
     ("simt_f32_d128", "f32", 1, 2, (150, 130), 128, 64, 4, 3.0, 1.0, 1.0),
     ("simt_f32_d64", "f32", 2, 2, (37, 100, 64), 64, 16, 4, 3.0, 1.0, 0.5),
-    ("simt_bf16_d64_w100", "bf16", 1, 2, (90, 160), 64, 100, 4, 3.0, 1.0, 1.0),
+    ("ws_d64_w100", "bf16", 1, 2, (90, 160), 64, 100, 4, 3.0, 1.0, 1.0),
     ("simt_f32_window_one", "f32", 1, 2, (50, 60), 64, 1, 2, 3.0, 1.0, 0.7),
     # head dim 256 (CUDA cores, value slices; the ring hand-off after the slices)
     ("simt_bf16_d256", "bf16", 1, 2, (70, 90, 5), 256, 64, 4, 3.0, 1.0, 1.0),

@@ -99,7 +99,11 @@ CASES = [
     ("d64_alpha_zero", "bf16", 1, 2, 190, 64, 64, 4, 3.0, 1.0, 0.0),
     ("d64_long_prompt_few_units", "bf16", 1, 2, 3000, 64, 64, 4, 3.0, 1.0, 0.7),
     ("d64_more_units_than_sms", "bf16", 5, 32, 70, 64, 64, 4, 3.0, 1.0, 1.0),
-    ("d64_w100_cuda_cores", "bf16", 1, 2, 300, 64, 100, 4, 3.0, 1.0, 1.0),
+    # head dim 64 with two earlier band chunks (windows 66..128)
+    ("d64_w100", "bf16", 1, 2, 300, 64, 100, 4, 3.0, 1.0, 1.0),
+    ("d64_w128_max_meta_strong_decay", "bf16", 1, 2, 333, 64, 128, 16, 0.0, 2.0, 0.5),
+    ("d64_w66_exact_intra", "bf16", 1, 2, 300, 64, 66, 4, -8.0, 4.0, 1.0),
+    ("d64_w120_L_below_w", "bf16", 2, 2, 40, 64, 120, 4, 3.0, 1.0, 1.0),
     # head dim 256 on the CUDA cores (four value slices per unit, 32-token chunks)
     ("d256_bf16_ragged", "bf16", 2, 2, 150, 256, 64, 4, 3.0, 1.0, 1.0),
     ("d256_f32_w128_max_meta", "f32", 1, 2, 170, 256, 128, 16, 0.0, 2.0, 0.5),

@@ -72,7 +72,7 @@ CASES = [
     ("simt_f32_gqa2", "f32", 1, 4, 2, 150, 64, 16, 4),
     ("ws_d64_mqa", "bf16", 2, 2, 1, 130, 64, 32, 3),
     ("ws_d64_gqa2", "bf16", 2, 4, 2, 200, 64, 64, 4),
-    ("simt_bf16_d64_w100_gqa2", "bf16", 1, 4, 2, 160, 64, 100, 4),
+    ("ws_d64_w100_gqa2", "bf16", 1, 4, 2, 160, 64, 100, 4),
     ("ws_per_head_alpha_only", "bf16", 1, 3, 3, 140, 128, 64, 4),
 ]
 
