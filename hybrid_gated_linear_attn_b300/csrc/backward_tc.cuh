@@ -1349,6 +1349,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int h0 = half * (C / 2), h1 = min(n, h0 + C / 2);
         {
             float sr = 0.f, sf = 0.f;
+#pragma unroll 8
             for (int t2 = h0; t2 < h1; ++t2) {
                 sr += bk[bx(t2, i)];
                 sf += yo[bx(t2, i)];
@@ -1361,11 +1362,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncthreads();
             float run = (half == 0 ? part[i] : 0.f) + E;  // reverse: later rows first
             float f = half == 1 ? part[128 + i] : 0.f;   // forward exclusive prefix
+#pragma unroll 8
             for (int t2 = h0; t2 < h1; ++t2) {  // forward prefix of k dk_inter, in place
                 const float x = yo[bx(t2, i)];
                 yo[bx(t2, i)] = f;
                 f += x;
             }
+#pragma unroll 8
             for (int t2 = h1 - 1; t2 >= h0; --t2) {
                 run += bk[bx(t2, i)];
                 if (i < d)
