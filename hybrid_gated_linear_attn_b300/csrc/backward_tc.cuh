@@ -761,47 +761,55 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // rounded exactly as the key side rounds it, so that the pairs
                 // that cancel in dlog gamma cancel to fp32 accuracy.
                 float gate[16], xg[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i = i0 + e;
-                    const float bt = bq[bx(t, i)];
-                    const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        sm + QO_Q + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
-                    const float inter = ex2(bt) * __uint_as_float(g1[e]);
-                    gate[e] = inter;
-                    xg[e] = qv * inter;
-                    if (!unsafe) {
-                        const float g2v = __uint_as_float(g2[e]);
-                        gate[e] += ex2(bt - rv[i]) * g2v;
-                        xg[e] += __bfloat162float(__float2bfloat16_rn(qv * ex2(bt - rv[i]))) * g2v;
-                    }
-                }
-                if (unsafe) {
-                    // exact: sum_{s<=t} dA[t][s] k_s[i] 2^{b_t[i] - b_s[i]} (every exponent <= 0)
-                    float intra[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) intra[e] = 0.f;
-                    for (int s2 = 0; s2 <= t; ++s2) {
-                        const float dA = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                            sm + QO_DA + sw128_offset(t, s2 * 2)));
-                        if (dA == 0.f) continue;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int i = i0 + e;
-                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                sm + QO_KC + (i / 64) * KB_K + sw128_offset(s2, (i % 64) * 2)));
-                            intra[e] += dA * kv * ex2(bq[bx(t, i)] - bq[bx(s2, i)]);
-                        }
-                    }
+                // The exact intra-chunk part of a wide chunk is a separate
+                // copy, so that the common one holds no rare code.
+                auto elems = [&](auto wide) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int i = i0 + e;
+                        const float bt = bq[bx(t, i)];
                         const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                             sm + QO_Q + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
-                        gate[e] += intra[e];
-                        xg[e] += qv * intra[e];
+                        const float inter = ex2(bt) * __uint_as_float(g1[e]);
+                        gate[e] = inter;
+                        xg[e] = qv * inter;
+                        if constexpr (!decltype(wide)::value) {
+                            const float g2v = __uint_as_float(g2[e]);
+                            gate[e] += ex2(bt - rv[i]) * g2v;
+                            xg[e] += __bfloat162float(__float2bfloat16_rn(qv * ex2(bt - rv[i]))) * g2v;
+                        }
                     }
-                }
+                    if constexpr (decltype(wide)::value) {
+                        // exact: sum_{s<=t} dA[t][s] k_s[i] 2^{b_t[i] - b_s[i]} (every exponent <= 0)
+                        float intra[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) intra[e] = 0.f;
+                        for (int s2 = 0; s2 <= t; ++s2) {
+                            const float dA = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                sm + QO_DA + sw128_offset(t, s2 * 2)));
+                            if (dA == 0.f) continue;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int i = i0 + e;
+                                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                    sm + QO_KC + (i / 64) * KB_K + sw128_offset(s2, (i % 64) * 2)));
+                                intra[e] += dA * kv * ex2(bq[bx(t, i)] - bq[bx(s2, i)]);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int i = i0 + e;
+                            const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                sm + QO_Q + (i / 64) * TILE + sw128_offset(t, (i % 64) * 2)));
+                            gate[e] += intra[e];
+                            xg[e] += qv * intra[e];
+                        }
+                    }
+                };
+                if (!unsafe)
+                    elems(std::false_type{});
+                else
+                    elems(std::true_type{});
                 const size_t row = (size_t)unit * L + c0 + t;
                 uint32_t pk[8];
 #pragma unroll
